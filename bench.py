@@ -1,0 +1,558 @@
+"""Benchmark: paged decode HBM GB/s and prefill TFLOP/s (K192/V128) on GB300.
+
+Headline step (``value``): one batched decode step of the library's hot path
+on the batched-decode workload (32 sequences, context U[2048, 8192], q_len 1,
+16 query / 4 KV heads, K 192 / V 128, block 16, bf16): write the step's new
+K/V into the paged cache, split-KV decode, merge.  ``value`` is the step's
+algorithmic HBM bytes (every visible K|V row once per KV head, Q, O, block
+table, and the write's reads and writes) per second of device time.  The
+KV cache (419 MB) is larger than L2, so no flush is needed between steps.
+
+Also reported (``sub``): causal prefill TFLOP/s at 32,768 tokens (and
+131,072 with --long), the cache write of 32,768 tokens, speculative verify
+with an FP8 cache (16 x ~46K, q_len 4, 16 splits, 8 padded rows) and the
+MLA-shaped decode (100K context, 12 and 16 heads, batch 1 and 16).  Those are
+timed per launch with L2 flushed between launches.
+
+``--impl reference`` times the CPU oracle (the reference arm of this build:
+no third-party implementation of this path runs on GB300) on a bounded sample
+of the same workload.  With several GPUs (torchrun), every rank runs an
+independent replica (the path has no exchange step): ``scaling`` is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode HBM GB/s & prefill TFLOP/s (K192/V128), % of GB300 roofline"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------- plumbing --
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself with one rank)."""
+    if ws <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed regions run."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    sources are unchanged since the capture (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("sha256"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# --------------------------------------------------- algorithmic counts --
+
+def decode_bytes(w) -> int:
+    """Visible K|V rows once per KV head (V inside K counted once), Q, O
+    (bf16) and the block-table entries read."""
+    e = 2 if w.kv_dtype == "bf16" else 1
+    lo = min(w.k_off, w.v_off)
+    hi = max(w.k_off + w.head_size, w.v_off + w.head_size_v)
+    kv = int(np.sum(w.seq_lens.astype(np.int64))) * w.num_kv_heads * (hi - lo) * e
+    q = w.num_tokens * w.num_q_heads * w.head_size * 2
+    o = w.num_tokens * w.num_q_heads * w.head_size_v * 2
+    bt = int(sum((int(L) + w.block_size - 1) // w.block_size for L in w.seq_lens)) * 4
+    return kv + q + o + bt
+
+
+def write_bytes(w, n_tokens: int) -> int:
+    e = 2 if w.kv_dtype == "bf16" else 1
+    per = w.num_kv_heads * (w.head_size + (w.head_size_v if w.v_ctx is not None else 0))
+    return n_tokens * (per * 2 + per * e + 8)
+
+
+def prefill_flops(w) -> float:
+    """2 * (dk + dv) multiply-adds per visible (query row, key) pair and
+    query head; masked pairs excluded."""
+    tot = 0
+    for b in range(w.num_seqs):
+        L, ql = int(w.seq_lens[b]), int(w.q_lens[b])
+        for_rows = 0
+        # keys seen by query i: clamp(L - ql + i + 1, 0, L)
+        first = L - ql + 1
+        lo_i = max(0, -first + 1)
+        n = ql - lo_i
+        a = first + lo_i
+        for_rows = n * a + n * (n - 1) // 2
+        tot += for_rows
+    return float(tot) * w.num_q_heads * 2 * (w.head_size + w.head_size_v)
+
+
+# ----------------------------------------------------------- GPU arm ----
+
+class Flusher:
+    def __init__(self, device):
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32,
+                               device=device)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_launches(fn, reps, warmup, flush=None):
+    """Mean device time (ms) of fn() over reps launches, events on the current
+    stream, L2 flushed between launches when a flusher is given."""
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.mean(ts), min(ts)
+
+
+def gpu_arm(args, ws, rank, local):
+    import paged_kv_asymmetric_gb300 as pkv
+    from paged_kv_asymmetric_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()  # raises if the library is not built
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    tf_burst = float(pk["bf16_tflops"])
+    launches = 0
+
+    # ---------------- headline: batched decode step -------------------
+    w = wl.batched_decode(seed=rank)
+    dw = wl.to_device(w, device=dev)
+    pkv.kv_cache_write(dw.k_ctx, dw.v_ctx, dw.slots_all, dw.cache)
+    S = w.max_splits
+    T, Hq, dv = w.num_tokens, w.num_q_heads, w.head_size_v
+    po = torch.empty(S, T, Hq, dv, dtype=torch.float32, device=dev)
+    pl = torch.empty(S, T, Hq, dtype=torch.float32, device=dev)
+    out = torch.empty(T, Hq, dv, dtype=torch.bfloat16, device=dev)
+    new_idx = dw.new_idx
+    k_new = dw.k_ctx[new_idx].contiguous()
+    v_new = dw.v_ctx[new_idx].contiguous()
+    stream = torch.cuda.current_stream()
+    dec_ev = []
+
+    def step(record=False):
+        pkv.kv_cache_write(k_new, v_new, dw.slots_new, dw.cache)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pkv.paged_attn_decode(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                              dw.query_start_loc, w.softmax_scale, 1, S,
+                              partial_o=po, partial_lse=pl)
+        if record:
+            e1.record(stream)
+            dec_ev.append((e0, e1))
+        pkv.splitkv_reduce(po, pl, out=out)
+
+    step_bytes = decode_bytes(w) + write_bytes(w, T)
+    for _ in range(max(3, args.warmup)):
+        step()
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ms_total = t0.elapsed_time(t1)
+    launches += 3 * args.steps
+    ms_total_max = max_over_ranks(ms_total, ws, dev)
+    ms_step = ms_total_max / args.steps
+    total_bytes = sum_over_ranks(step_bytes * args.steps, ws, dev)
+    value = total_bytes / (ms_total_max * 1e-3) / 1e9
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    dec_alg = decode_bytes(w)
+    dec_gbs = dec_alg / (dec_ms * 1e-3) / 1e9
+
+    # ---------------- e2e: host buffers through the public API ---------
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_k, h_v = pin(dw.q), pin(k_new), pin(v_new)
+    h_slots, h_bt = pin(dw.slots_new), pin(dw.block_table)
+    h_sl, h_qsl = pin(dw.seq_lens), pin(dw.query_start_loc)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(dw.q), torch.empty_like(k_new), torch.empty_like(v_new)
+    d_slots, d_bt = torch.empty_like(dw.slots_new), torch.empty_like(dw.block_table)
+    d_sl, d_qsl = torch.empty_like(dw.seq_lens), torch.empty_like(dw.query_start_loc)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_sl, h_qsl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots),
+                     (d_bt, h_bt), (d_sl, h_sl), (d_qsl, h_qsl)):
+            d.copy_(h, non_blocking=True)
+        pkv.kv_cache_write(d_k, d_v, d_slots, dw.cache)
+        pkv.paged_attn_decode(d_q, dw.cache, d_bt, d_sl, d_qsl,
+                              w.softmax_scale, 1, S, partial_o=po,
+                              partial_lse=pl)
+        pkv.splitkv_reduce(po, pl, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
+    launches += 3 * args.steps
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+
+    # ---------------- sub-measurements --------------------------------
+    flush = Flusher(dev)
+    sub = {}
+    reps = max(3, args.sub_reps)
+
+    def attn_decode_sub(name, wk, splits):
+        dwk = wl.to_device(wk, device=dev)
+        pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
+                           dwk.k_scale, dwk.v_scale)
+        Tk, Hk, dvk = wk.num_tokens, wk.num_q_heads, wk.head_size_v
+        pok = torch.empty(splits, Tk, Hk, dvk, dtype=torch.float32, device=dev)
+        plk = torch.empty(splits, Tk, Hk, dtype=torch.float32, device=dev)
+        outk = torch.empty(Tk, Hk, dvk, dtype=torch.bfloat16, device=dev)
+
+        def dec():
+            pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
+                                  dwk.seq_lens, dwk.query_start_loc,
+                                  wk.softmax_scale, wk.max_query_len, splits,
+                                  partial_o=pok, partial_lse=plk,
+                                  k_scale=dwk.k_scale, v_scale=dwk.v_scale)
+
+        def red():
+            pkv.splitkv_reduce(pok, plk, out=outk)
+        md, _ = time_launches(dec, reps, 2, flush)
+        mr, _ = time_launches(red, reps, 2, flush)
+        b = decode_bytes(wk)
+        sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
+                     "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
+                     "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
+                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm}
+        del dwk, pok, plk, outk
+        torch.cuda.empty_cache()
+
+    def prefill_sub(name, n_tokens):
+        wk = wl.long_prefill(n_tokens, device=dev)
+        dwk = wl.to_device(wk, device=dev)
+        nw = wk.k_ctx.shape[0]
+
+        def wr():
+            pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache)
+        mw, _ = time_launches(wr, reps, 2, flush)
+        wb = write_bytes(wk, nw)
+        outk = torch.empty(wk.num_tokens, wk.num_q_heads, wk.head_size_v,
+                           dtype=torch.bfloat16, device=dev)
+
+        def pf():
+            pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
+                                   dwk.seq_lens, dwk.query_start_loc,
+                                   wk.softmax_scale, out=outk)
+        mp, _ = time_launches(pf, reps, 2, flush)
+        fl = prefill_flops(wk)
+        sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
+                     "TFLOPs": fl / (mp * 1e-3) / 1e12,
+                     "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
+                     "write_ms": mw, "write_bytes": wb,
+                     "write_GBps": wb / (mw * 1e-3) / 1e9,
+                     "write_frac_hbm": wb / (mw * 1e-3) / 1e9 / hbm}
+        del dwk, outk
+        torch.cuda.empty_cache()
+
+    if not args.no_sub:
+        if not args.skip_prefill:
+            prefill_sub("prefill_32k", 32768)
+            if args.long:
+                prefill_sub("prefill_128k", 131072)
+        wv = wl.verify_fp8(device=dev)
+        attn_decode_sub("verify_fp8", wv, 16)
+        del wv
+        for b in (1, 16):
+            for h in (12, 16):
+                wm = wl.mla_decode(batch=b, heads=h, device=dev)
+                s = pkv.decode_suggest_splits(b, h, 1, 1, 100000, 64)
+                attn_decode_sub(f"mla_b{b}_h{h}", wm, s)
+                del wm
+    clocks = sampler.stop()
+
+    traffic = traffic_record("decode_bf16_192")
+    roof = {"kernel": "decode_kernel<192,128,bf16>", "bound": "hbm",
+            "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+            "frac": dec_gbs / hbm, "peak_kind": pk_kind,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": dec_alg,
+            "avg_launch_ms": dec_ms}
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), random page placement)",
+        "config": {"workload": "batched-decode: 32 seqs, ctx U[2048,8192], q_len 1, "
+                   "Hq16/Hkv4, K192/V128, block 16, bf16, 16 splits",
+                   "step": "kv_cache_write(new tokens) + paged_attn_decode + splitkv_reduce",
+                   "l2": "inputs larger than L2 (419 MB KV cache)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "sub": sub,
+    }
+    if "prefill_32k" in sub:
+        p = sub["prefill_32k"]
+        res["prefill_tflops"] = p["TFLOPs"]
+        res["roofline_prefill"] = {
+            "kernel": "prefill_kernel (tcgen05)", "bound": "tensor",
+            "achieved": p["TFLOPs"], "peak": tf_burst, "unit": "TFLOP/s",
+            "frac": p["frac_bf16"], "peak_kind": pk_kind,
+            "traffic": traffic_record("prefill"), "avg_launch_ms": p["prefill_ms"]}
+    return res
+
+
+# ------------------------------------------------------ oracle (CPU) ----
+
+def oracle_decode_sample(target_s: float, seed: int = 0, nseq: int = 0):
+    """The oracle on the first `nseq` sequences of the batched-decode workload:
+    build its cache once, then repeat (write the step's new tokens, attend for
+    the step's query rows) until about target_s seconds have passed."""
+    import oracle
+    from paged_kv_asymmetric_gb300 import workloads as wl
+    from tests import refs
+
+    w = wl.batched_decode(seed=seed)
+    if nseq <= 0:  # one query row per host core, at most the whole batch
+        nseq = max(1, min(w.num_seqs, os.cpu_count() or 1))
+    seqs = list(range(nseq))
+    cache = refs.oracle_cache(w, seqs=seqs)
+    threads = os.cpu_count() or 1
+    d = refs.oracle_desc(w)
+    toks = np.arange(nseq, dtype=np.int32)
+    kb, vb = refs.bf16_bits(w.k_ctx), refs.bf16_bits(w.v_ctx)
+    idx = w.new_kv_index()[:nseq]
+    slots = w.slot_mapping_new()[:nseq]
+    sub_bytes = 0
+    e = 2
+    for b in seqs:
+        sub_bytes += int(w.seq_lens[b]) * w.num_kv_heads * w.row_elems * e
+    sub_bytes += nseq * w.num_q_heads * (w.head_size + w.head_size_v) * 2
+    sub_bytes += write_bytes(w, nseq)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.kv_cache_write(kb[idx], vb[idx], slots, cache, d)
+        refs.oracle_attn(w, cache, tokens=toks, threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or n >= 1000:
+            break
+    return {"value": sub_bytes * n / el / 1e9, "unit": "GB/s",
+            "cores": min(threads, nseq),
+            "kind": "oracle",
+            "sample": f"first {nseq} of 32 sequences of the batched-decode step "
+                      f"(write + attention, threads over query rows), {n} "
+                      f"repetitions in {el:.1f} s",
+            "seconds_per_step": el / n}
+
+
+def reference_arm(args, ws, rank):
+    if rank != 0:
+        return None
+    base = oracle_decode_sample(target_s=max(2.0, args.ref_seconds / max(1, args.steps)))
+    vals = []
+    for _ in range(args.steps):
+        vals.append(oracle_decode_sample(
+            target_s=max(1.0, args.ref_seconds / max(1, args.steps)))["value"])
+    v = statistics.mean(vals)
+    return {
+        "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": base["seconds_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded N(0,1), random page placement)",
+        "config": {"workload": "batched-decode: 32 seqs, ctx U[2048,8192], q_len 1, "
+                   "Hq16/Hkv4, K192/V128, block 16, bf16, 16 splits",
+                   "step": "oracle: kv_cache_write(new tokens) + paged attention",
+                   "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": base["cores"],
+                         "kind": "oracle", "sample": base["sample"]},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--long", action="store_true", help="add the 131,072-token prefill")
+    ap.add_argument("--no-sub", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--sub-reps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=30.0)
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_info()
+    if args.impl == "reference":
+        init_dist(ws, "gloo")
+        res = reference_arm(args, ws, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    init_dist(ws, "nccl")
+    res = gpu_arm(args, ws, rank, local)
+    if rank == 0:
+        if ws == 1:
+            res["cpu_baseline"] = oracle_decode_sample(args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,251 @@
+/*
+ * pkv.h -- C ABI of the paged-KV attention library for GB300 (sm_103a):
+ * block-paged KV cache with asymmetric K/V head sizes (K 192 / V 128 with
+ * GQA, and the MLA shape 576 / 512 where V is a prefix of K).
+ *
+ * Sources the operations follow (web pages, by title and section):
+ *   - vLLM PR #64064 "ROCm AITER unified attention for MiMo-V2.6":
+ *     "Details" -- reshape_and_cache_flash writes V with V's own head size
+ *     and head stride; one packed (head_size + head_size_v) row per KV head,
+ *     K first; "Tests" -- block sizes 16 and 64, two cache layouts, bf16 and
+ *     fp8 caches, per-tensor and per-head scales; "Details" / "Known
+ *     limitations" -- a backend that splits the page at head_size serves
+ *     v <= k only.
+ *   - vLLM PR #50371 "Enable 12-head MLA persistent decode": "Purpose" and
+ *     "Test Plan" (12 query heads, one latent head, D 576 -> 512) and the
+ *     discussion of split-KV with split selection from device-side sequence
+ *     metadata (launch shape stays graph-stable).
+ *   - Hugging Face model card "diffbot/MiMo-V2.6-Flash-MOPD-FP8KV-W4A8-2x-
+ *     RTX-PRO-6000": "What the kernels do" (split-KV for the speculative
+ *     verify step, FP8 E4M3 K/V converted in the kernel, a prefill attention
+ *     kernel for the global layers) and "Update 2026-10-01" (a query row with
+ *     no visible key is 0, not NaN, after the split-KV merge).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory and performs no host<->device
+ *     synchronisation, except pkv_get_device_error, which says so.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns a status: PKV_OK (0) or a negative
+ *     PKV_E* code.  Arguments are validated on the host before anything is
+ *     launched; a rejected call launches nothing.  PKV_ECUDA means a launch
+ *     failed; pkv_last_cuda_error() returns the cudaError_t value.
+ *   - bf16 tensors are IEEE bfloat16; fp8 is OCP FP8 E4M3 ("e4m3fn":
+ *     saturating, max 448, no infinities).
+ *   - Sequences: sequence b has q_len(b) = query_start_loc[b+1] -
+ *     query_start_loc[b] query tokens and seq_lens[b] keys in total, the
+ *     query tokens' own keys included (they are written to the cache first).
+ *     Query i of the sequence sits at position seq_lens[b] - q_len(b) + i and
+ *     attends to keys 0 .. that position (causal, bottom-right aligned).  Key
+ *     j of sequence b lives in page block_table[b * max_blocks_per_seq +
+ *     j / block_size] at offset j % block_size.  Only the first
+ *     ceil(seq_lens[b] / block_size) entries of a block-table row are read.
+ *   - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Out-of-range slots or page ids met on the device are not dereferenced:
+ *     the element is skipped (write) or read as zero (attention) and the
+ *     device error word records PKV_EDEV_RANGE (see pkv_get_device_error).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pkv_stream_t; /* the same type as cudaStream_t */
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_EINVAL (-1)        /* null pointer, size or stride out of range */
+#define PKV_EUNSUPPORTED (-2)  /* valid, but a shape / dtype this build lacks */
+#define PKV_ECUDA (-3)         /* a CUDA launch or query failed */
+
+/* device error word values (pkv_get_device_error) */
+#define PKV_EDEV_NONE 0
+#define PKV_EDEV_RANGE 1       /* slot or page id out of range: skipped */
+#define PKV_EDEV_TIMEOUT 2     /* a bounded wait in a kernel gave up */
+
+/* cache element types */
+#define PKV_BF16 0
+#define PKV_FP8_E4M3 1
+
+/* cache layouts; R = row_elems */
+#define PKV_NHD 0              /* [num_blocks][block_size][num_kv_heads][R] */
+#define PKV_HND 1              /* [num_blocks][num_kv_heads][block_size][R] */
+
+/* fp8 scale modes (bf16 caches take PKV_SCALE_NONE) */
+#define PKV_SCALE_NONE 0
+#define PKV_SCALE_TENSOR 1     /* k_scale[0], v_scale[0] */
+#define PKV_SCALE_HEAD 2       /* k_scale[h], v_scale[h], h < num_kv_heads */
+
+/*
+ * One block-paged cache (vLLM PR #64064, "Details").  Every (slot, KV head)
+ * owns one row of row_elems elements; K occupies [k_off, k_off + head_size)
+ * and V occupies [v_off, v_off + head_size_v).  MiMo: row 320, K at 0 (192),
+ * V at 192 (128).  MLA: row 576, K at 0 (576), V at 0 (512) -- V is a prefix
+ * of K and is never written separately.
+ */
+typedef struct pkv_cache_desc {
+    int dtype;        /* PKV_BF16 | PKV_FP8_E4M3 */
+    int layout;       /* PKV_NHD | PKV_HND */
+    int num_blocks;   /* pages in the cache */
+    int block_size;   /* tokens per page, >= 1 */
+    int num_kv_heads;
+    int row_elems;    /* R */
+    int k_off, head_size;
+    int v_off, head_size_v;
+    int scale_mode;   /* PKV_SCALE_* */
+} pkv_cache_desc;
+
+/*
+ * pkv_kv_cache_write -- vLLM PR #64064, "Details" (the asymmetric branch of
+ * reshape_and_cache_flash).
+ *
+ * For every token t < num_tokens with s = slot_mapping[t] >= 0, and every
+ * KV head h: row = the (s / block_size, s % block_size, h) row of `cache`;
+ *   row[k_off + i] = enc_k(key[t * key_tok_stride + h * key_head_stride + i])
+ *                    for i < head_size,
+ *   row[v_off + i] = enc_v(value[t * val_tok_stride + h * val_head_stride + i])
+ *                    for i < head_size_v (skipped when value == NULL).
+ * Strides are in elements.  A negative slot skips the token.  No other byte of
+ * the cache is written.  enc is a bit copy for a bf16 cache; for an fp8 cache
+ * it is E4M3(x / scale) with the division in IEEE binary32, round-to-nearest-
+ * even and saturation to +-448 (NaN stays NaN).  key/value: bf16.  slot_mapping:
+ * int64 [num_tokens].  k_scale / v_scale: device float32, [1] or
+ * [num_kv_heads] by d->scale_mode (NULL for bf16 caches).  When V is a prefix
+ * of K (value == NULL), read it back with v_scale equal to k_scale.
+ * Errors: PKV_EINVAL for null pointers (key, slot_mapping, cache, d; scales
+ * when required), negative sizes, K or V ranges outside the row, num_tokens <
+ * 0; PKV_EUNSUPPORTED for an unknown dtype / layout / scale mode.
+ */
+int pkv_kv_cache_write(const void *key, int64_t key_tok_stride,
+                       int64_t key_head_stride, const void *value,
+                       int64_t val_tok_stride, int64_t val_head_stride,
+                       const int64_t *slot_mapping, int num_tokens,
+                       void *cache, const pkv_cache_desc *d,
+                       const float *k_scale, const float *v_scale,
+                       pkv_stream_t stream);
+
+/*
+ * pkv_paged_attn_prefill -- causal varlen attention of a batch of query
+ * chunks over the paged cache (the prefill rows of the MiMo model card's
+ * "What the kernels do"; semantics of vLLM PR #64064's unified attention).
+ *
+ * out[t][h][:] = sum_j softmax_j(softmax_scale * q[t][h] . K_j) * V_j over the
+ * keys j the query token sees (see the sequence conventions above).  q: bf16
+ * [num_tokens][num_q_heads][head_size]; out: bf16
+ * [num_tokens][num_q_heads][head_size_v]; block_table: int32
+ * [num_seqs][max_blocks_per_seq]; seq_lens: int32 [num_seqs];
+ * query_start_loc: int32 [num_seqs + 1], non-decreasing, last = num_tokens.
+ * seq_lens[b] >= q_len(b) is required for every row to see a key; a row that
+ * sees none is written as 0.  The K and V of every visible key must already
+ * be in the cache.  Keys past seq_lens[b] in the last page are never used,
+ * whatever the cache holds there.
+ * softmax_scale must be > 0.  k_scale / v_scale as in the write (fp8
+ * caches; NULL for bf16).
+ * This build: bf16 cache, head_size 192 and head_size_v 128, num_q_heads /
+ * num_kv_heads dividing 128, block_size a power of two >= 8, K at a
+ * 64-element column offset; otherwise PKV_EUNSUPPORTED.  PKV_EINVAL for null
+ * pointers, softmax_scale <= 0 or inconsistent sizes.
+ */
+int pkv_paged_attn_prefill(const void *q, int num_q_heads, int num_tokens,
+                           const void *cache, const pkv_cache_desc *d,
+                           const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *seq_lens,
+                           const int32_t *query_start_loc, int num_seqs,
+                           float softmax_scale, const float *k_scale,
+                           const float *v_scale, void *out,
+                           pkv_stream_t stream);
+
+/*
+ * pkv_paged_attn_decode -- split-KV decode and speculative verify (q_len 1
+ * .. max_query_len) over the paged cache: the verify-step split-KV of the
+ * MiMo model card's "What the kernels do", the 12-head MLA decode of vLLM
+ * PR #50371 ("Purpose"), split selection from device-side sequence lengths
+ * with a graph-stable launch shape (vLLM PR #50371 discussion).
+ *
+ * The P = ceil(seq_lens[b] / block_size) pages of sequence b are cut into
+ * num_splits segments of pps = ceil(P / num_splits) pages; segment s covers
+ * pages [s * pps, min((s + 1) * pps, P)).  For every query row (t, h) and
+ * segment s, over the keys of the segment that the row sees:
+ *   partial_lse[s][t][h]  = log(sum_j exp(softmax_scale * q . K_j))  (natural
+ *                           log; -inf when the segment has no such key),
+ *   partial_o[s][t][h][:] = sum_j softmax_j * V_j  (normalised within the
+ *                           segment; left unwritten when partial_lse is -inf).
+ * K and V are dequantised with k_scale / v_scale for fp8 caches.  Merge the
+ * segments with pkv_splitkv_reduce.  partial_o: float32
+ * [num_splits][num_tokens][num_q_heads][head_size_v]; partial_lse: float32
+ * [num_splits][num_tokens][num_q_heads].  Other arguments as in prefill.
+ * A sequence with seq_lens[b] == 0 (a padded row) gives -inf everywhere; its
+ * block-table row is never read.  max_query_len bounds q_len(b) for the
+ * launch shape (1 .. 64).
+ * This build: head_size / head_size_v 192 / 128 (bf16 or fp8 cache) or
+ * 576 / 512 (bf16 or fp8 cache); otherwise PKV_EUNSUPPORTED.
+ */
+int pkv_paged_attn_decode(const void *q, int num_q_heads, int num_tokens,
+                          const void *cache, const pkv_cache_desc *d,
+                          const int32_t *block_table, int max_blocks_per_seq,
+                          const int32_t *seq_lens,
+                          const int32_t *query_start_loc, int num_seqs,
+                          int max_query_len, float softmax_scale,
+                          const float *k_scale, const float *v_scale,
+                          int num_splits, float *partial_o,
+                          float *partial_lse, pkv_stream_t stream);
+
+/*
+ * pkv_splitkv_reduce -- the split-KV merge (MiMo model card, "What the
+ * kernels do" and "Update 2026-10-01").
+ *
+ * For each row r < num_rows: M = max_s partial_lse[s][r].  If M is -inf, or
+ * num_splits is 0, out[r][:] = 0 and lse_out[r] = -inf (never NaN).
+ * Otherwise w_s = exp(partial_lse[s][r] - M) (segments at -inf are skipped
+ * and their partial_o is not read), out[r][:] = sum_s w_s * partial_o[s][r][:]
+ * / sum_s w_s, rounded to bf16, and lse_out[r] = M + log(sum_s w_s).
+ * partial_o: float32 [num_splits][num_rows][head_size_v]; partial_lse:
+ * float32 [num_splits][num_rows]; out: bf16 [num_rows][head_size_v];
+ * lse_out: float32 [num_rows] or NULL.  For the decode call, num_rows =
+ * num_tokens * num_q_heads.
+ */
+int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
+                       int num_splits, int num_rows, int head_size_v,
+                       void *out, float *lse_out, pkv_stream_t stream);
+
+/*
+ * pkv_decode_suggest_splits -- a split count that gives the decode launch
+ * about two CTAs per SM of the current device, for sequences of up to
+ * max_seq_len keys, capped so that every segment keeps at least one page.
+ * Host-only; returns >= 1, or a negative status.
+ */
+int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
+                              int max_query_len, int max_seq_len,
+                              int block_size);
+
+/*
+ * pkv_supports -- whether this build serves a K/V head-size pair for a cache
+ * dtype in each call: bit 0 write, bit 1 prefill, bit 2 decode.  Mirrors the
+ * per-backend capability check of vLLM PR #64064 ("Details": v <= k is what
+ * a page split at head_size can serve); 0 when v > k.
+ */
+int pkv_supports(int head_size, int head_size_v, int dtype);
+
+/*
+ * pkv_get_device_error -- reads and clears the library's device error word
+ * (PKV_EDEV_*), ordering the read after all work queued on `stream`.  This
+ * call synchronises `stream`.  Returns PKV_OK or PKV_ECUDA.
+ */
+int pkv_get_device_error(int *code, pkv_stream_t stream);
+
+/* The cudaError_t of the last PKV_ECUDA return on the calling thread. */
+int pkv_last_cuda_error(void);
+
+/* A static description of a status code. */
+const char *pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

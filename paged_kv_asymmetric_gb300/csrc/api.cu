@@ -1,0 +1,357 @@
+// api.cu -- the C ABI declared in include/pkv.h: host-side argument checks
+// (everything is checked before anything is launched), the device error word
+// and the launches.  No call allocates device memory or synchronises, except
+// pkv_get_device_error.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// The device error word (PKV_EDEV_*).  Kernels receive its address; host
+// code reads it only through pkv_get_device_error.
+__device__ int g_pkv_dev_error = 0;
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+int g_num_sms[kMaxDevices] = {0};
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return PKV_ECUDA;
+}
+
+// Per-device constants: the device address of the error word and the SM
+// count.  Resolved once per device, with that device current.
+int device_info(int** err_ptr, int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return fail_cuda(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_pkv_dev_error);
+    if (e != cudaSuccess) return fail_cuda(e);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  if (err_ptr) *err_ptr = g_err_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return PKV_OK;
+}
+
+int check_desc(const pkv_cache_desc* d) {
+  if (d == nullptr) return PKV_EINVAL;
+  if (d->dtype != PKV_BF16 && d->dtype != PKV_FP8_E4M3) return PKV_EUNSUPPORTED;
+  if (d->layout != PKV_NHD && d->layout != PKV_HND) return PKV_EUNSUPPORTED;
+  if (d->scale_mode < PKV_SCALE_NONE || d->scale_mode > PKV_SCALE_HEAD)
+    return PKV_EUNSUPPORTED;
+  if (d->num_blocks < 1 || d->block_size < 1 || d->num_kv_heads < 1 ||
+      d->row_elems < 1 || d->head_size < 1 || d->head_size_v < 1 ||
+      d->k_off < 0 || d->v_off < 0)
+    return PKV_EINVAL;
+  if (static_cast<int64_t>(d->k_off) + d->head_size > d->row_elems ||
+      static_cast<int64_t>(d->v_off) + d->head_size_v > d->row_elems)
+    return PKV_EINVAL;
+  if (d->dtype == PKV_BF16 && d->scale_mode != PKV_SCALE_NONE) return PKV_EINVAL;
+  if (d->dtype == PKV_FP8_E4M3 && d->scale_mode == PKV_SCALE_NONE)
+    return PKV_EINVAL;
+  return PKV_OK;
+}
+
+int check_attn_common(const void* q, int num_q_heads, int num_tokens,
+                      const void* cache, const pkv_cache_desc* d,
+                      const int32_t* block_table, int max_blocks_per_seq,
+                      const int32_t* seq_lens, const int32_t* qsl,
+                      int num_seqs, float softmax_scale, const float* k_scale,
+                      const float* v_scale) {
+  int rc = check_desc(d);
+  if (rc != PKV_OK) return rc;
+  if (d->head_size_v > d->head_size) return PKV_EUNSUPPORTED;
+  if (num_tokens < 0 || num_seqs < 0 || num_q_heads < 1) return PKV_EINVAL;
+  if (num_q_heads % d->num_kv_heads != 0) return PKV_EINVAL;
+  if (!isfinite(softmax_scale)) return PKV_EINVAL;
+  if (num_tokens > 0 && q == nullptr) return PKV_EINVAL;
+  if (cache == nullptr || qsl == nullptr) return PKV_EINVAL;
+  if (num_seqs > 0 &&
+      (block_table == nullptr || seq_lens == nullptr || max_blocks_per_seq < 1))
+    return PKV_EINVAL;
+  if (d->dtype == PKV_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr))
+    return PKV_EINVAL;
+  return PKV_OK;
+}
+
+pkv::AttnParams make_params(const void* q, int num_q_heads, int num_tokens,
+                            const void* cache, const pkv_cache_desc* d,
+                            const int32_t* block_table, int max_blocks_per_seq,
+                            const int32_t* seq_lens, const int32_t* qsl,
+                            int num_seqs, float softmax_scale,
+                            const float* k_scale, const float* v_scale,
+                            int* err) {
+  pkv::AttnParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.cache = cache;
+  p.dtype = d->dtype;
+  p.layout = d->layout;
+  p.num_blocks = d->num_blocks;
+  p.block_size = d->block_size;
+  p.num_kv_heads = d->num_kv_heads;
+  p.row_elems = d->row_elems;
+  p.k_off = d->k_off;
+  p.head_size = d->head_size;
+  p.v_off = d->v_off;
+  p.head_size_v = d->head_size_v;
+  p.scale_mode = d->scale_mode;
+  p.block_table = block_table;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.query_start_loc = qsl;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.num_q_heads = num_q_heads;
+  p.group = num_q_heads / d->num_kv_heads;
+  p.softmax_scale = softmax_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = err;
+  return p;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_kv_cache_write(const void* key, int64_t key_tok_stride,
+                       int64_t key_head_stride, const void* value,
+                       int64_t val_tok_stride, int64_t val_head_stride,
+                       const int64_t* slot_mapping, int num_tokens, void* cache,
+                       const pkv_cache_desc* d, const float* k_scale,
+                       const float* v_scale, pkv_stream_t stream) {
+  int rc = check_desc(d);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (key == nullptr || slot_mapping == nullptr || cache == nullptr)
+    return PKV_EINVAL;
+  if (key_tok_stride < 0 || key_head_stride < 0 || val_tok_stride < 0 ||
+      val_head_stride < 0)
+    return PKV_EINVAL;
+  if (d->dtype == PKV_FP8_E4M3 &&
+      (k_scale == nullptr || (value != nullptr && v_scale == nullptr)))
+    return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  rc = device_info(&err, &sms);
+  if (rc != PKV_OK) return rc;
+  pkv::WriteParams p{};
+  p.key = static_cast<const __nv_bfloat16*>(key);
+  p.value = static_cast<const __nv_bfloat16*>(value);
+  p.key_tok_stride = key_tok_stride;
+  p.key_head_stride = key_head_stride;
+  p.val_tok_stride = val_tok_stride;
+  p.val_head_stride = val_head_stride;
+  p.slot_mapping = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.has_value = value != nullptr;
+  p.cache = cache;
+  p.dtype = d->dtype;
+  p.layout = d->layout;
+  p.num_blocks = d->num_blocks;
+  p.block_size = d->block_size;
+  p.num_kv_heads = d->num_kv_heads;
+  p.row_elems = d->row_elems;
+  p.k_off = d->k_off;
+  p.head_size = d->head_size;
+  p.v_off = d->v_off;
+  p.head_size_v = d->head_size_v;
+  p.scale_mode = d->scale_mode;
+  p.k_scale = k_scale;
+  p.v_scale = value != nullptr ? v_scale : k_scale;
+  p.err = err;
+  cudaError_t e = pkv::launch_cache_write(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
+                           const void* cache, const pkv_cache_desc* d,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* seq_lens,
+                           const int32_t* query_start_loc, int num_seqs,
+                           float softmax_scale, const float* k_scale,
+                           const float* v_scale, void* out,
+                           pkv_stream_t stream) {
+  int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
+                             max_blocks_per_seq, seq_lens, query_start_loc,
+                             num_seqs, softmax_scale, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens > 0 && out == nullptr) return PKV_EINVAL;
+  if (!(softmax_scale > 0.f)) return PKV_EINVAL;
+  if (!pkv::prefill_supported(d->head_size, d->head_size_v, d->dtype))
+    return PKV_EUNSUPPORTED;
+  const int G = num_q_heads / d->num_kv_heads;
+  if (128 % G != 0) return PKV_EUNSUPPORTED;
+  const int bs = d->block_size;
+  if (bs < 8 || (bs & (bs - 1)) != 0) return PKV_EUNSUPPORTED;
+  // TMA tiles: 16-byte aligned base and row strides, 64-element K/V boxes
+  if (!aligned16(cache) || !aligned16(q) || (d->row_elems * 2) % 16 != 0 ||
+      d->k_off % 64 != 0 || d->v_off % 8 != 0)
+    return PKV_EUNSUPPORTED;
+  if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
+  int* err = nullptr;
+  int sms = 0;
+  rc = device_info(&err, &sms);
+  if (rc != PKV_OK) return rc;
+  pkv::AttnParams p = make_params(q, num_q_heads, num_tokens, cache, d,
+                                  block_table, max_blocks_per_seq, seq_lens,
+                                  query_start_loc, num_seqs, softmax_scale,
+                                  k_scale, v_scale, err);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  cudaError_t e = pkv::launch_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
+                          const void* cache, const pkv_cache_desc* d,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens,
+                          const int32_t* query_start_loc, int num_seqs,
+                          int max_query_len, float softmax_scale,
+                          const float* k_scale, const float* v_scale,
+                          int num_splits, float* partial_o, float* partial_lse,
+                          pkv_stream_t stream) {
+  int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
+                             max_blocks_per_seq, seq_lens, query_start_loc,
+                             num_seqs, softmax_scale, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (max_query_len < 1 || max_query_len > 64) return PKV_EINVAL;
+  if (num_splits < 1 || num_splits > 65535) return PKV_EINVAL;
+  if (num_tokens > 0 && (partial_o == nullptr || partial_lse == nullptr))
+    return PKV_EINVAL;
+  if (!pkv::decode_supported(d->head_size, d->head_size_v, d->dtype))
+    return PKV_EUNSUPPORTED;
+  const int esz = d->dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const int lo = d->k_off < d->v_off ? d->k_off : d->v_off;
+  const int hi_k = d->k_off + d->head_size, hi_v = d->v_off + d->head_size_v;
+  const int span = (hi_k > hi_v ? hi_k : hi_v) - lo;
+  const int max_span = d->head_size == 192 ? 320 : 576;
+  // 16-byte cp.async pieces: the staged span, its start and the K / V starts
+  // within it are whole pieces; rows and the cache base are 16-byte aligned.
+  if (span > max_span || (span * esz) % 16 != 0 || (lo * esz) % 16 != 0 ||
+      ((d->k_off - lo) * esz) % 16 != 0 || ((d->v_off - lo) * esz) % 16 != 0 ||
+      (static_cast<int64_t>(d->row_elems) * esz) % 16 != 0 ||
+      !aligned16(cache) || !aligned16(q))
+    return PKV_EUNSUPPORTED;
+  const int G = num_q_heads / d->num_kv_heads;
+  const int64_t row_groups = (static_cast<int64_t>(max_query_len) * G + 15) / 16;
+  if (row_groups * d->num_kv_heads > 65535 || num_seqs > 65535)
+    return PKV_EINVAL;
+  if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
+  int* err = nullptr;
+  rc = device_info(&err, nullptr);
+  if (rc != PKV_OK) return rc;
+  pkv::AttnParams p = make_params(q, num_q_heads, num_tokens, cache, d,
+                                  block_table, max_blocks_per_seq, seq_lens,
+                                  query_start_loc, num_seqs, softmax_scale,
+                                  k_scale, v_scale, err);
+  p.max_query_len = max_query_len;
+  p.num_splits = num_splits;
+  p.partial_o = partial_o;
+  p.partial_lse = partial_lse;
+  cudaError_t e = pkv::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_splitkv_reduce(const float* partial_o, const float* partial_lse,
+                       int num_splits, int num_rows, int head_size_v, void* out,
+                       float* lse_out, pkv_stream_t stream) {
+  if (num_splits < 0 || num_rows < 0 || head_size_v < 1) return PKV_EINVAL;
+  if (num_rows == 0) return PKV_OK;
+  if (out == nullptr) return PKV_EINVAL;
+  if (num_splits > 0 && (partial_o == nullptr || partial_lse == nullptr))
+    return PKV_EINVAL;
+  if ((head_size_v & 3) == 0 &&
+      ((reinterpret_cast<uintptr_t>(partial_o) & 15u) != 0 ||
+       (reinterpret_cast<uintptr_t>(out) & 7u) != 0))
+    return PKV_EINVAL;
+  cudaError_t e = pkv::launch_splitkv_reduce(
+      partial_o, partial_lse, num_splits, num_rows, head_size_v,
+      static_cast<__nv_bfloat16*>(out), lse_out,
+      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
+                              int max_query_len, int max_seq_len,
+                              int block_size) {
+  if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
+      max_query_len < 1 || max_seq_len < 0 || block_size < 1 ||
+      num_q_heads % num_kv_heads != 0)
+    return PKV_EINVAL;
+  int sms = 0;
+  int rc = device_info(nullptr, &sms);
+  if (rc != PKV_OK) return rc;
+  const int64_t G = num_q_heads / num_kv_heads;
+  const int64_t ctas = static_cast<int64_t>(num_seqs) * num_kv_heads *
+                       ((max_query_len * G + 15) / 16);
+  int64_t s = (2 * static_cast<int64_t>(sms) + ctas - 1) / ctas;
+  const int64_t pages = (static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size;
+  if (s > pages) s = pages;
+  if (s < 1) s = 1;
+  if (s > 1024) s = 1024;
+  return static_cast<int>(s);
+}
+
+int pkv_supports(int head_size, int head_size_v, int dtype) {
+  if (head_size < 1 || head_size_v < 1 || head_size_v > head_size) return 0;
+  if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return 0;
+  int bits = 1;  // the write takes any K / V sizes
+  if (pkv::prefill_supported(head_size, head_size_v, dtype)) bits |= 2;
+  if (pkv::decode_supported(head_size, head_size_v, dtype)) bits |= 4;
+  return bits;
+}
+
+int pkv_get_device_error(int* code, pkv_stream_t stream) {
+  if (code == nullptr) return PKV_EINVAL;
+  int* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc != PKV_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  *code = host;
+  return PKV_OK;
+}
+
+int pkv_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_EUNSUPPORTED: return "unsupported shape, dtype or layout";
+    case PKV_ECUDA: return "CUDA error (see pkv_last_cuda_error)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// kernels.h -- internal launch interfaces between the C ABI (api.cu) and the
+// kernels.  Not installed; the public interface is include/pkv.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+struct WriteParams {
+  const __nv_bfloat16* key;
+  const __nv_bfloat16* value;
+  int64_t key_tok_stride, key_head_stride;
+  int64_t val_tok_stride, val_head_stride;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  int has_value;
+  void* cache;
+  int dtype, layout, num_blocks, block_size, num_kv_heads, row_elems;
+  int k_off, head_size, v_off, head_size_v, scale_mode;
+  const float* k_scale;
+  const float* v_scale;
+  int* err;
+};
+
+// Shared by the decode and prefill kernels.
+struct AttnParams {
+  const __nv_bfloat16* q;      // [T][Hq][dk]
+  const void* cache;
+  int dtype, layout, num_blocks, block_size, num_kv_heads, row_elems;
+  int k_off, head_size, v_off, head_size_v, scale_mode;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int num_seqs;
+  int num_tokens;
+  int num_q_heads;
+  int group;                   // Hq / Hkv
+  int max_query_len;
+  float softmax_scale;
+  const float* k_scale;
+  const float* v_scale;
+  // decode
+  int num_splits;
+  float* partial_o;            // [S][T][Hq][dv]
+  float* partial_lse;          // [S][T][Hq]
+  // prefill
+  __nv_bfloat16* out;          // [T][Hq][dv]
+  int* err;
+};
+
+cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
+                               cudaStream_t stream);
+
+// Returns cudaErrorNotSupported for a shape without an instantiation.
+cudaError_t launch_decode(const AttnParams& p, cudaStream_t stream);
+bool decode_supported(int head_size, int head_size_v, int dtype);
+
+cudaError_t launch_splitkv_reduce(const float* partial_o,
+                                  const float* partial_lse, int num_splits,
+                                  int num_rows, int head_size_v,
+                                  __nv_bfloat16* out, float* lse_out,
+                                  cudaStream_t stream);
+
+cudaError_t launch_prefill(const AttnParams& p, int num_sms,
+                           cudaStream_t stream);
+bool prefill_supported(int head_size, int head_size_v, int dtype);
+
+}  // namespace pkv

@@ -1,0 +1,109 @@
+// reduce.cu -- the split-KV merge (MiMo-V2.6-Flash 2x RTX PRO 6000 model
+// card, "What the kernels do" and "Update 2026-10-01"): each row's segment
+// partials (o_s, lse_s) are combined with weights exp(lse_s - max lse); a row
+// whose segments are all empty is written as 0 with lse -inf instead of the
+// exp(-inf - -inf) = NaN the unclamped merge produces.
+//
+// One warp per row: the split weights are recomputed by every lane from the
+// (broadcast) lse values, and each lane accumulates four consecutive output
+// columns per pass with 16-byte loads.  The kernel reads S * dv * 4 bytes per
+// row and writes dv * 2; it is small next to the decode it follows.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+    splitkv_reduce_kernel(const float* __restrict__ po,
+                          const float* __restrict__ plse, int S, int rows,
+                          int dv, __nv_bfloat16* __restrict__ out,
+                          float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const bool vec = (dv & 3) == 0;
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows;
+       r += gridDim.x * wpb) {
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32)
+      M = fmaxf(M, __ldg(plse + static_cast<int64_t>(s) * rows + r));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
+    if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
+      for (int c = lane; c < dv; c += 32) orow[c] = __float2bfloat16_rn(0.f);
+      if (lse_out != nullptr && lane == 0) lse_out[r] = -INFINITY;
+      continue;
+    }
+    const float Ml2 = M * kLog2e;
+    float W = 0.f;
+    if (vec) {
+      for (int c0 = 0; c0 < dv; c0 += 128) {
+        const int c = c0 + 4 * lane;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        for (int s = 0; s < S; ++s) {
+          const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
+          if (x == -INFINITY) continue;  // empty segment: o_s is not read
+          const float w = fast_exp2(fmaf(x, kLog2e, -Ml2));
+          wsum += w;
+          if (c < dv) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(
+                po + (static_cast<int64_t>(s) * rows + r) * dv + c));
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+          }
+        }
+        W = wsum;
+        if (c < dv) {
+          const float inv = 1.f / wsum;
+          uint2 st;
+          st.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+          st.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(orow + c) = st;
+        }
+      }
+    } else {
+      for (int c = lane; c < dv; c += 32) {
+        float acc = 0.f, wsum = 0.f;
+        for (int s = 0; s < S; ++s) {
+          const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
+          if (x == -INFINITY) continue;
+          const float w = fast_exp2(fmaf(x, kLog2e, -Ml2));
+          wsum += w;
+          acc = fmaf(w, __ldg(po + (static_cast<int64_t>(s) * rows + r) * dv + c),
+                     acc);
+        }
+        W = wsum;
+        orow[c] = __float2bfloat16_rn(acc / wsum);
+      }
+    }
+    if (lse_out != nullptr && lane == 0) {
+      lse_out[r] = M + fast_log2(W) * kLn2;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_splitkv_reduce(const float* partial_o,
+                                  const float* partial_lse, int num_splits,
+                                  int num_rows, int head_size_v,
+                                  __nv_bfloat16* out, float* lse_out,
+                                  cudaStream_t stream) {
+  if (num_rows == 0) return cudaSuccess;
+  const int wpb = 8;
+  int blocks = (num_rows + wpb - 1) / wpb;
+  if (blocks > 65535) blocks = 65535;
+  splitkv_reduce_kernel<<<blocks, 32 * wpb, 0, stream>>>(
+      partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -251,3 +251,64 @@ def mla_decode(batch: int = 1, heads: int = 12, ctx: int = 100_000,
                          block_size=64, v_aliases_k=True,
                          softmax_scale=1.0 / math.sqrt(576), seed=seed,
                          max_splits=64, device=device)
+
+
+# ------------------------------------------------------ device marshalling --
+
+@dataclasses.dataclass
+class DeviceWorkload:
+    """The tensors of a workload on a CUDA device, ready for the library."""
+    w: Workload
+    cache: object            # paged_kv_asymmetric_gb300.Cache
+    cache_buf: torch.Tensor  # uint8 storage: slack | cache | slack
+    slack: int
+    q: torch.Tensor
+    k_ctx: torch.Tensor
+    v_ctx: Optional[torch.Tensor]
+    slots_all: torch.Tensor
+    slots_new: torch.Tensor
+    new_idx: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    query_start_loc: torch.Tensor
+    k_scale: Optional[torch.Tensor]
+    v_scale: Optional[torch.Tensor]
+
+
+def desc_of(w: Workload):
+    from paged_kv_asymmetric_gb300 import (BF16 as _B, FP8_E4M3 as _F,
+                                           NHD as _N, HND as _H, make_desc)
+    return make_desc(
+        dtype=_B if w.kv_dtype == BF16 else _F,
+        layout=_N if w.layout == NHD else _H, num_blocks=w.num_blocks,
+        block_size=w.block_size, num_kv_heads=w.num_kv_heads,
+        row_elems=w.row_elems, k_off=w.k_off, head_size=w.head_size,
+        v_off=w.v_off, head_size_v=w.head_size_v,
+        scale_mode={SCALE_NONE: 0, SCALE_TENSOR: 1, SCALE_HEAD: 2}[w.scale_mode])
+
+
+def to_device(w: Workload, device="cuda", fill_byte: int = 0xFF,
+              slack: int = 4096) -> DeviceWorkload:
+    """Copies a workload to the device.  The cache is allocated with `slack`
+    guard bytes on both sides and every byte (guards included) set to
+    fill_byte (0xFF reads as NaN in both bf16 and E4M3, so an unwritten slot
+    that leaked into a result would show)."""
+    from paged_kv_asymmetric_gb300 import Cache
+    d = desc_of(w)
+    nbytes = w.cache_bytes()
+    buf = torch.full((nbytes + 2 * slack,), fill_byte, dtype=torch.uint8,
+                     device=device)
+    cache = Cache(buf[slack:slack + nbytes], d)
+    f32 = lambda a: None if a is None else torch.from_numpy(
+        np.asarray(a, dtype=np.float32)).to(device)
+    return DeviceWorkload(
+        w=w, cache=cache, cache_buf=buf, slack=slack,
+        q=w.q.to(device).contiguous(), k_ctx=w.k_ctx.to(device),
+        v_ctx=None if w.v_ctx is None else w.v_ctx.to(device),
+        slots_all=torch.from_numpy(w.slot_mapping_all()).to(device),
+        slots_new=torch.from_numpy(w.slot_mapping_new()).to(device),
+        new_idx=torch.from_numpy(w.new_kv_index()).to(device),
+        block_table=torch.from_numpy(w.block_table).to(device),
+        seq_lens=torch.from_numpy(w.seq_lens).to(device),
+        query_start_loc=torch.from_numpy(w.query_start_loc).to(device),
+        k_scale=f32(w.k_scale), v_scale=f32(w.v_scale))

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/pkv.h declares, and rejects bad arguments on the host before
+anything is launched (the checks below never reach a CUDA call)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_asymmetric_gb300 as pkv
+from paged_kv_asymmetric_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("pkv_kv_cache_write", "pkv_paged_attn_prefill",
+              "pkv_paged_attn_decode", "pkv_splitkv_reduce"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(_declared()) <= set(pkv.EXPORTED) | {"pkv_status_string"}
+
+
+def test_supports_mirrors_v_le_k(lib):
+    assert pkv.supports(192, 128) == 7
+    assert pkv.supports(192, 128, pkv.FP8_E4M3) == 5   # no fp8 prefill yet
+    assert pkv.supports(576, 512) == 5
+    assert pkv.supports(128, 192) == 0                  # V wider than K
+    assert pkv.supports(64, 64) == 1                    # write only
+
+
+def _desc(**kw):
+    base = dict(num_blocks=4)
+    base.update(kw)
+    return pkv.make_desc(**base)
+
+
+DUMMY = ctypes.c_void_p(256)   # never dereferenced: validation fails first
+
+
+def _write(lib, d, key=DUMMY, slots=DUMMY, cache=DUMMY, T=1, ks=None, vs=None,
+           value=DUMMY):
+    return lib.pkv_kv_cache_write(key, 192, 192 * 0 + 192, value, 128, 128,
+                                  slots, T, cache,
+                                  None if d is None else ctypes.byref(d),
+                                  ks, vs, None)
+
+
+def test_write_rejects_bad_arguments(lib):
+    assert _write(lib, None) == pkv.EINVAL
+    assert _write(lib, _desc(), key=None) == pkv.EINVAL
+    assert _write(lib, _desc(), slots=None) == pkv.EINVAL
+    assert _write(lib, _desc(), T=-1) == pkv.EINVAL
+    assert _write(lib, _desc(dtype=7)) == pkv.EUNSUPPORTED
+    assert _write(lib, _desc(layout=5)) == pkv.EUNSUPPORTED
+    assert _write(lib, _desc(v_off=250)) == pkv.EINVAL        # V past the row
+    assert _write(lib, _desc(dtype=pkv.FP8_E4M3,
+                             scale_mode=pkv.SCALE_HEAD)) == pkv.EINVAL  # no scales
+    assert _write(lib, _desc(scale_mode=pkv.SCALE_TENSOR)) == pkv.EINVAL
+    assert _write(lib, _desc(), T=0) == pkv.OK                # nothing to do
+
+
+def _decode(lib, d, **kw):
+    a = dict(q=DUMMY, Hq=16, T=4, cache=DUMMY, bt=DUMMY, mb=4, sl=DUMMY,
+             qsl=DUMMY, B=2, mq=1, scale=0.1, ks=None, vs=None, S=4,
+             po=DUMMY, pl=DUMMY)
+    a.update(kw)
+    return lib.pkv_paged_attn_decode(
+        a["q"], a["Hq"], a["T"], a["cache"],
+        None if d is None else ctypes.byref(d), a["bt"], a["mb"], a["sl"],
+        a["qsl"], a["B"], a["mq"], ctypes.c_float(a["scale"]), a["ks"],
+        a["vs"], a["S"], a["po"], a["pl"], None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    d = _desc()
+    assert _decode(lib, None) == pkv.EINVAL
+    assert _decode(lib, _desc(head_size=128, head_size_v=192, v_off=128,
+                              row_elems=320)) == pkv.EUNSUPPORTED  # v > k
+    assert _decode(lib, d, Hq=15) == pkv.EINVAL          # Hq % Hkv
+    assert _decode(lib, d, S=0) == pkv.EINVAL
+    assert _decode(lib, d, mq=0) == pkv.EINVAL
+    assert _decode(lib, d, mq=65) == pkv.EINVAL
+    assert _decode(lib, d, po=None) == pkv.EINVAL
+    assert _decode(lib, d, bt=None) == pkv.EINVAL
+    assert _decode(lib, d, scale=float("nan")) == pkv.EINVAL
+    assert _decode(lib, _desc(head_size=64, head_size_v=64, row_elems=128,
+                              v_off=64)) == pkv.EUNSUPPORTED
+    assert _decode(lib, _desc(dtype=pkv.FP8_E4M3,
+                              scale_mode=pkv.SCALE_TENSOR)) == pkv.EINVAL
+    assert _decode(lib, d, T=0) == pkv.OK
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    def call(d, **kw):
+        a = dict(q=DUMMY, Hq=16, T=4, scale=0.1, out=DUMMY)
+        a.update(kw)
+        return lib.pkv_paged_attn_prefill(
+            a["q"], a["Hq"], a["T"], DUMMY, ctypes.byref(d), DUMMY, 4, DUMMY,
+            DUMMY, 1, ctypes.c_float(a["scale"]), None, None, a["out"], None)
+    assert call(_desc(), scale=-1.0) == pkv.EINVAL
+    assert call(_desc(), out=None) == pkv.EINVAL
+    assert call(_desc(block_size=12)) == pkv.EUNSUPPORTED
+    assert call(_desc(), Hq=12 * 4 * 3) in (pkv.EUNSUPPORTED,)  # G = 36
+    assert call(_desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)) == \
+        pkv.EINVAL   # scales missing
+
+
+def test_reduce_rejects_bad_arguments(lib):
+    f = lib.pkv_splitkv_reduce
+    assert f(DUMMY, DUMMY, -1, 4, 128, DUMMY, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 4, 0, DUMMY, None, None) == pkv.EINVAL
+    assert f(None, DUMMY, 2, 4, 128, DUMMY, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 4, 128, None, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 0, 128, None, None, None) == pkv.OK
+
+
+def test_status_strings(lib):
+    for s in (pkv.OK, pkv.EINVAL, pkv.EUNSUPPORTED, pkv.ECUDA):
+        assert lib.pkv_status_string(s)
