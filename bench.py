@@ -245,6 +245,81 @@ def gpu_arm(args, ws, rank, local):
     tf_burst = float(pk["bf16_tflops"])
     launches = 0
 
+    # ---------------- sub-measurements --------------------------------
+    flush = Flusher(dev)
+    sub = {}
+    reps = max(3, args.sub_reps)
+
+    def attn_decode_sub(name, wk, splits):
+        dwk = wl.to_device(wk, device=dev)
+        pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
+                           dwk.k_scale, dwk.v_scale)
+        Tk, Hk, dvk = wk.num_tokens, wk.num_q_heads, wk.head_size_v
+        pok = torch.empty(splits, Tk, Hk, dvk, dtype=torch.float32, device=dev)
+        plk = torch.empty(splits, Tk, Hk, dtype=torch.float32, device=dev)
+        outk = torch.empty(Tk, Hk, dvk, dtype=torch.bfloat16, device=dev)
+
+        def dec():
+            pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
+                                  dwk.seq_lens, dwk.query_start_loc,
+                                  wk.softmax_scale, wk.max_query_len, splits,
+                                  partial_o=pok, partial_lse=plk,
+                                  k_scale=dwk.k_scale, v_scale=dwk.v_scale)
+
+        def red():
+            pkv.splitkv_reduce(pok, plk, out=outk)
+        md, _ = time_launches(dec, reps, 2, flush)
+        mr, _ = time_launches(red, reps, 2, flush)
+        b = decode_bytes(wk)
+        sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
+                     "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
+                     "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
+                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm}
+        del dwk, pok, plk, outk
+        torch.cuda.empty_cache()
+
+    def prefill_sub(name, n_tokens):
+        wk = wl.long_prefill(n_tokens, device=dev)
+        dwk = wl.to_device(wk, device=dev)
+        nw = wk.k_ctx.shape[0]
+
+        def wr():
+            pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache)
+        mw, _ = time_launches(wr, reps, 2, flush)
+        wb = write_bytes(wk, nw)
+        outk = torch.empty(wk.num_tokens, wk.num_q_heads, wk.head_size_v,
+                           dtype=torch.bfloat16, device=dev)
+
+        def pf():
+            pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
+                                   dwk.seq_lens, dwk.query_start_loc,
+                                   wk.softmax_scale, out=outk)
+        mp, _ = time_launches(pf, reps, 2, flush)
+        fl = prefill_flops(wk)
+        sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
+                     "TFLOPs": fl / (mp * 1e-3) / 1e12,
+                     "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
+                     "write_ms": mw, "write_bytes": wb,
+                     "write_GBps": wb / (mw * 1e-3) / 1e9,
+                     "write_frac_hbm": wb / (mw * 1e-3) / 1e9 / hbm}
+        del dwk, outk
+        torch.cuda.empty_cache()
+
+    if args.only:
+        sampler = ClockSampler(local)
+        sampler.start()
+        if args.only == "prefill":
+            prefill_sub(f"prefill_{args.prefill_tokens}", args.prefill_tokens)
+        elif args.only == "verify":
+            attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), 16)
+        elif args.only == "mla":
+            s = pkv.decode_suggest_splits(1, 16, 1, 1, 100000, 64)
+            attn_decode_sub("mla_b1_h16", wl.mla_decode(batch=1, heads=16,
+                                                        device=dev), s)
+        elif args.only == "decode":
+            attn_decode_sub("batched_decode", wl.batched_decode(device=dev), 16)
+        return {"only": args.only, "sub": sub, "clocks": sampler.stop()}
+
     # ---------------- headline: batched decode step -------------------
     w = wl.batched_decode(seed=rank)
     dw = wl.to_device(w, device=dev)
@@ -337,66 +412,6 @@ def gpu_arm(args, ws, rank, local):
     e2e_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
     launches += 3 * args.steps
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
-
-    # ---------------- sub-measurements --------------------------------
-    flush = Flusher(dev)
-    sub = {}
-    reps = max(3, args.sub_reps)
-
-    def attn_decode_sub(name, wk, splits):
-        dwk = wl.to_device(wk, device=dev)
-        pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
-                           dwk.k_scale, dwk.v_scale)
-        Tk, Hk, dvk = wk.num_tokens, wk.num_q_heads, wk.head_size_v
-        pok = torch.empty(splits, Tk, Hk, dvk, dtype=torch.float32, device=dev)
-        plk = torch.empty(splits, Tk, Hk, dtype=torch.float32, device=dev)
-        outk = torch.empty(Tk, Hk, dvk, dtype=torch.bfloat16, device=dev)
-
-        def dec():
-            pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
-                                  dwk.seq_lens, dwk.query_start_loc,
-                                  wk.softmax_scale, wk.max_query_len, splits,
-                                  partial_o=pok, partial_lse=plk,
-                                  k_scale=dwk.k_scale, v_scale=dwk.v_scale)
-
-        def red():
-            pkv.splitkv_reduce(pok, plk, out=outk)
-        md, _ = time_launches(dec, reps, 2, flush)
-        mr, _ = time_launches(red, reps, 2, flush)
-        b = decode_bytes(wk)
-        sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
-                     "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
-                     "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
-                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm}
-        del dwk, pok, plk, outk
-        torch.cuda.empty_cache()
-
-    def prefill_sub(name, n_tokens):
-        wk = wl.long_prefill(n_tokens, device=dev)
-        dwk = wl.to_device(wk, device=dev)
-        nw = wk.k_ctx.shape[0]
-
-        def wr():
-            pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache)
-        mw, _ = time_launches(wr, reps, 2, flush)
-        wb = write_bytes(wk, nw)
-        outk = torch.empty(wk.num_tokens, wk.num_q_heads, wk.head_size_v,
-                           dtype=torch.bfloat16, device=dev)
-
-        def pf():
-            pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
-                                   dwk.seq_lens, dwk.query_start_loc,
-                                   wk.softmax_scale, out=outk)
-        mp, _ = time_launches(pf, reps, 2, flush)
-        fl = prefill_flops(wk)
-        sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
-                     "TFLOPs": fl / (mp * 1e-3) / 1e12,
-                     "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
-                     "write_ms": mw, "write_bytes": wb,
-                     "write_GBps": wb / (mw * 1e-3) / 1e9,
-                     "write_frac_hbm": wb / (mw * 1e-3) / 1e9 / hbm}
-        del dwk, outk
-        torch.cuda.empty_cache()
 
     if not args.no_sub:
         if not args.skip_prefill:
@@ -530,6 +545,9 @@ def main(argv=None):
     ap.add_argument("--long", action="store_true", help="add the 131,072-token prefill")
     ap.add_argument("--no-sub", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "verify", "mla", "decode"],
+                    help="run one sub-measurement alone (for profiling)")
+    ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--sub-reps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=30.0)
@@ -546,7 +564,7 @@ def main(argv=None):
     init_dist(ws, "nccl")
     res = gpu_arm(args, ws, rank, local)
     if rank == 0:
-        if ws == 1:
+        if ws == 1 and not args.only:
             res["cpu_baseline"] = oracle_decode_sample(args.cpu_seconds)
         print(json.dumps(res), flush=True)
     if ws > 1:

@@ -261,9 +261,12 @@ int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
   const int64_t row_groups = (static_cast<int64_t>(max_query_len) * G + 15) / 16;
   if (row_groups * d->num_kv_heads > 65535 || num_seqs > 65535)
     return PKV_EINVAL;
+  // 16-key chunks are whole TMA boxes of one page (or two pages of 8)
+  if (!(d->block_size % 16 == 0 || d->block_size == 8)) return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
   int* err = nullptr;
-  rc = device_info(&err, nullptr);
+  int sms = 0;
+  rc = device_info(&err, &sms);
   if (rc != PKV_OK) return rc;
   pkv::AttnParams p = make_params(q, num_q_heads, num_tokens, cache, d,
                                   block_table, max_blocks_per_seq, seq_lens,
@@ -273,7 +276,7 @@ int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
   p.num_splits = num_splits;
   p.partial_o = partial_o;
   p.partial_lse = partial_lse;
-  cudaError_t e = pkv::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = pkv::launch_decode(p, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }

@@ -57,7 +57,7 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
                                cudaStream_t stream);
 
 // Returns cudaErrorNotSupported for a shape without an instantiation.
-cudaError_t launch_decode(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream);
 bool decode_supported(int head_size, int head_size_v, int dtype);
 
 cudaError_t launch_splitkv_reduce(const float* partial_o,

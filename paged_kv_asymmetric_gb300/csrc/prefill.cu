@@ -157,33 +157,46 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int box_rows = bs < BN ? bs : BN;
   const int nbox = BN / box_rows;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------ TMA producer ------
+    // The whole warp runs this loop.  Lane i owns box i of a 128-key slab
+    // (nbox <= 16 boxes, one page or part of one each): it loads that box's
+    // page id two tiles ahead of use and issues the box's copy itself, so
+    // page-table reads never sit between consecutive copies.
     uint32_t qi = 0, f = 0;
     bool ok = true;
-    auto fill_slab = [&](const Item& it, int kt, int col) -> bool {
+    const int32_t* bt_row = nullptr;
+    auto load_pid = [&](const Item& it, int kt) -> int {
+      const int key0 = kt * BN + lane * box_rows;
+      if (kt >= it.ntiles || lane >= nbox || key0 >= it.L) return -1;
+      return __ldg(bt_row + key0 / bs);
+    };
+    auto fill_slab = [&](const Item& it, int kt, int col, int pid) -> bool {
       const uint32_t slot = f % NSLAB;
-      if (!tc5::mbar_wait(bar(B_SLAB_EMPTY0 + slot), ((f / NSLAB) & 1u) ^ 1u,
-                          abort_flag, p.err))
-        return false;
+      bool w = true;
+      if (lane == 0)
+        w = tc5::mbar_wait(bar(B_SLAB_EMPTY0 + slot), ((f / NSLAB) & 1u) ^ 1u,
+                           abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, w, 0)) return false;
       const int lim = it.L - kt * BN;  // keys of the tile inside the sequence
       const int nb = min(nbox, (lim + box_rows - 1) / box_rows);
       const uint32_t full = bar(B_SLAB_FULL0 + slot);
-      tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * 128));
-      const uint32_t dst = sbase + RING_OFF + slot * SLAB;
-      const int32_t* bt = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
-      for (int pb = 0; pb < nb; ++pb) {
-        const int key0 = kt * BN + pb * box_rows;
-        int page = __ldg(bt + key0 / bs);
+      if (lane == 0)
+        tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * 128));
+      __syncwarp();
+      if (lane < nb) {
+        const int key0 = kt * BN + lane * box_rows;
         const int off = key0 % bs;
+        int page = pid;
         if (page < 0 || page >= p.num_blocks) {
           set_dev_error(p.err, PKV_EDEV_RANGE);
           page = p.num_blocks;  // out-of-range box: TMA fills zeros
         }
+        const uint32_t dst = sbase + RING_OFF + slot * SLAB + lane * box_rows * 128;
         if (p.layout == PKV_NHD)
-          tc5::tma_load_4d(dst + pb * box_rows * 128, &kv_map, col, it.g, off, page, full);
+          tc5::tma_load_4d(dst, &kv_map, col, it.g, off, page, full);
         else
-          tc5::tma_load_4d(dst + pb * box_rows * 128, &kv_map, col, off, it.g, page, full);
+          tc5::tma_load_4d(dst, &kv_map, col, off, it.g, page, full);
       }
       ++f;
       return true;
@@ -192,26 +205,41 @@ __global__ void __launch_bounds__(THREADS, 1)
       Item it;
       if (!get_item(p, TQ, idx, it)) break;
       if (it.ntiles == 0) continue;
-      if (!tc5::mbar_wait(bar(B_QEMPTY), (qi & 1u) ^ 1u, abort_flag, p.err)) break;
-      tc5::mbar_arrive_expect_tx(bar(B_QFULL), KSLABS * SLAB);
-      for (int c = 0; c < KSLABS; ++c)
-        tc5::tma_load_3d(sbase + Q_OFF + c * SLAB, &q_map, 64 * c, it.g * G, it.q0,
-                         bar(B_QFULL));
+      bt_row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
+      int pid0 = load_pid(it, 0), pid1 = load_pid(it, 1);
+      bool w = true;
+      if (lane == 0) {
+        w = tc5::mbar_wait(bar(B_QEMPTY), (qi & 1u) ^ 1u, abort_flag, p.err);
+        if (w) {
+          tc5::mbar_arrive_expect_tx(bar(B_QFULL), KSLABS * SLAB);
+          for (int c = 0; c < KSLABS; ++c)
+            tc5::tma_load_3d(sbase + Q_OFF + c * SLAB, &q_map, 64 * c, it.g * G,
+                             it.q0, bar(B_QFULL));
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, w, 0)) break;
       ++qi;
-      for (int c = 0; c < KSLABS && ok; ++c) ok = fill_slab(it, 0, p.k_off + 64 * c);
+      for (int c = 0; c < KSLABS && ok; ++c) ok = fill_slab(it, 0, p.k_off + 64 * c, pid0);
       for (int j = 0; j < it.ntiles && ok; ++j) {
+        const int pid2 = load_pid(it, j + 2);  // prefetch
         if (j + 1 < it.ntiles)
-          for (int c = 0; c < KSLABS && ok; ++c) ok = fill_slab(it, j + 1, p.k_off + 64 * c);
-        for (int h = 0; h < VSLABS && ok; ++h) ok = fill_slab(it, j, p.v_off + 64 * h);
+          for (int c = 0; c < KSLABS && ok; ++c)
+            ok = fill_slab(it, j + 1, p.k_off + 64 * c, pid1);
+        for (int h = 0; h < VSLABS && ok; ++h) ok = fill_slab(it, j, p.v_off + 64 * h, pid0);
+        pid0 = pid1;
+        pid1 = pid2;
       }
     }
     // Outstanding copies land before the CTA may exit (they all have on the
     // normal path; after an abort some may still be in flight).
-    for (uint32_t k = f > NSLAB ? f - NSLAB : 0; k < f; ++k)
-      tc5::mbar_wait(bar(B_SLAB_FULL0 + k % NSLAB), (k / NSLAB) & 1u, abort_flag,
-                     p.err, /*honor_abort=*/false);
-    if (qi > 0)
-      tc5::mbar_wait(bar(B_QFULL), (qi - 1) & 1u, abort_flag, p.err, false);
+    if (lane == 0) {
+      for (uint32_t k = f > NSLAB ? f - NSLAB : 0; k < f; ++k)
+        tc5::mbar_wait(bar(B_SLAB_FULL0 + k % NSLAB), (k / NSLAB) & 1u, abort_flag,
+                       p.err, /*honor_abort=*/false);
+      if (qi > 0)
+        tc5::mbar_wait(bar(B_QFULL), (qi - 1) & 1u, abort_flag, p.err, false);
+    }
+    __syncwarp();
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer --------
     constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(BM, BN, false);
@@ -324,13 +352,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc5::tc_fence_after();
         float s[BN];
+        {
+          uint32_t v[BN / 32][32];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tc5::tmem_ld_32x32b_x32(tmem + lane_off + TM_S0 + buf * BN + 32 * c, v);
+          for (int c = 0; c < BN / 32; ++c)
+            tc5::tmem_ld_32x32b_x32(tmem + lane_off + TM_S0 + buf * BN + 32 * c, v[c]);
           tc5::tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(v[k]);
+          for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(v[c][k]);
         }
         tc5::tc_fence_before();
         tc5::mbar_arrive(bar(B_SFREE0 + buf));

@@ -90,6 +90,104 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// One CTA per row for rows with many splits or wide V (dv % 4 == 0): the
+// split maxima and weight sums are block reductions, and the threads form
+// `ngrp` groups over the splits x `cols` lanes over 16-byte column pieces, so
+// that a row with hundreds of splits is read by hundreds of loads in flight
+// instead of one warp's serial walk.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+    splitkv_reduce_rows_kernel(const float* __restrict__ po,
+                               const float* __restrict__ plse, int S, int rows,
+                               int dv, __nv_bfloat16* __restrict__ out,
+                               float* __restrict__ lse_out) {
+  __shared__ float red[THREADS / 32];
+  __shared__ float4 part[THREADS];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int r = blockIdx.x;
+  auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, u) : v + u;
+    }
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+  };
+  float M = -INFINITY;
+  for (int s = tid; s < S; s += THREADS)
+    M = fmaxf(M, __ldg(plse + static_cast<int64_t>(s) * rows + r));
+  M = block_reduce(M, true);
+  __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
+  if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
+    for (int c = tid; c < dv; c += THREADS) orow[c] = __float2bfloat16_rn(0.f);
+    if (lse_out != nullptr && tid == 0) lse_out[r] = -INFINITY;
+    return;
+  }
+  const float Ml2 = M * kLog2e;
+  float wsum = 0.f;
+  for (int s = tid; s < S; s += THREADS) {
+    const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
+    if (x != -INFINITY) wsum += fast_exp2(fmaf(x, kLog2e, -Ml2));
+  }
+  const float W = block_reduce(wsum, false);
+  const float inv = 1.f / W;
+  const int dv4 = dv >> 2;
+  const int cols = dv4 < THREADS ? dv4 : THREADS;
+  const int ngrp = THREADS / cols;
+  const int c = tid % cols, grp = tid / cols;
+  for (int c0 = 0; c0 < dv4; c0 += cols) {
+    const int c4 = c0 + c;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (grp < ngrp && c4 < dv4) {
+      // four splits per step, their loads independent of each other
+      constexpr int U = 4;
+      for (int s0 = grp; s0 < S; s0 += U * ngrp) {
+        float w[U];
+        float4 v[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int s = s0 + k * ngrp;
+          const float x = s < S ? __ldg(plse + static_cast<int64_t>(s) * rows + r)
+                                : -INFINITY;
+          // an empty segment's o_s is not read
+          w[k] = x == -INFINITY ? 0.f : fast_exp2(fmaf(x, kLog2e, -Ml2));
+          v[k] = w[k] != 0.f
+                     ? __ldg(reinterpret_cast<const float4*>(
+                                 po + (static_cast<int64_t>(s) * rows + r) * dv) + c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          acc.x = fmaf(w[k], v[k].x, acc.x);
+          acc.y = fmaf(w[k], v[k].y, acc.y);
+          acc.z = fmaf(w[k], v[k].z, acc.z);
+          acc.w = fmaf(w[k], v[k].w, acc.w);
+        }
+      }
+    }
+    __syncthreads();
+    part[tid] = acc;
+    __syncthreads();
+    if (grp == 0 && c4 < dv4) {
+      for (int g2 = 1; g2 < ngrp; ++g2) {
+        const float4 v = part[g2 * cols + c];
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      uint2 st;
+      st.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      st.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(orow + 4 * c4) = st;
+    }
+  }
+  if (lse_out != nullptr && tid == 0) lse_out[r] = M + fast_log2(W) * kLn2;
+}
+
 }  // namespace
 
 cudaError_t launch_splitkv_reduce(const float* partial_o,
@@ -98,6 +196,11 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
                                   __nv_bfloat16* out, float* lse_out,
                                   cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
+  if ((head_size_v & 3) == 0) {
+    splitkv_reduce_rows_kernel<512><<<num_rows, 512, 0, stream>>>(
+        partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out);
+    return cudaGetLastError();
+  }
   const int wpb = 8;
   int blocks = (num_rows + wpb - 1) / wpb;
   if (blocks > 65535) blocks = 65535;

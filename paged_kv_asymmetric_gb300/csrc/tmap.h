@@ -1,0 +1,79 @@
+// tmap.h -- host-side construction of TMA tensor maps over the block-paged
+// cache (and over row-major Q), shared by the prefill and decode launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pkv.h"
+
+namespace pkv {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A 4-D map over the cache whose boxes are `box_cols` row elements wide (one
+// 128-byte swizzle span) and `box_rows` token slots high, for one KV head of
+// one page.  Coordinates: NHD (col, head, slot, page), HND (col, slot, head,
+// page).  Columns past row_elems read as zero.
+inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
+                            int layout, int num_blocks, int block_size,
+                            int num_kv_heads, int row_elems, int box_cols,
+                            int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encode_fn();
+  if (encode == nullptr) return false;
+  const cuuint64_t e = dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const cuuint64_t R = static_cast<cuuint64_t>(row_elems);
+  const cuuint64_t H = static_cast<cuuint64_t>(num_kv_heads);
+  const cuuint64_t B = static_cast<cuuint64_t>(block_size);
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  if (layout == PKV_NHD) {  // [blk][bs][H][R]
+    dims[0] = R; dims[1] = H; dims[2] = B; dims[3] = static_cast<cuuint64_t>(num_blocks);
+    strides[0] = R * e; strides[1] = H * R * e; strides[2] = B * H * R * e;
+    box[0] = box_cols; box[1] = 1; box[2] = box_rows; box[3] = 1;
+  } else {                  // [blk][H][bs][R]
+    dims[0] = R; dims[1] = B; dims[2] = H; dims[3] = static_cast<cuuint64_t>(num_blocks);
+    strides[0] = R * e; strides[1] = B * R * e; strides[2] = H * B * R * e;
+    box[0] = box_cols; box[1] = box_rows; box[2] = 1; box[3] = 1;
+  }
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode(map,
+                dtype == PKV_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                4, const_cast<void*>(cache), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sets the dynamic shared-memory limit of `fn` once per device.
+template <class F>
+inline cudaError_t ensure_smem_attr(F* fn, int bytes, int* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !done[dev]) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = 1;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace pkv
