@@ -20,7 +20,7 @@
 //    K and V pages as 64-column boxes of one page each into 128-key slabs of
 //    an 8-slab ring; page ids prefetched two tiles ahead by all lanes),
 //    warp 1 issues tcgen05.mma from one thread, warps 4..7 run the softmax
-//    with one thread per query row, alternating between tiles A and B.
+//    of tile A and warps 8..11 that of tile B, one thread per query row.
 //  * Tensor memory holds S and O of both tiles (4 x 128 columns).  The
 //    tensor core works on one tile while the softmax works on the other:
 //    S_A(j) and S_B(j) = Q K_j^T (M 128, N 128, K 192, operands in shared
@@ -73,7 +73,7 @@ enum {
 };
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem base, abort word
 constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;  // 4 control warps + 2 softmax warpgroups
 constexpr uint32_t TMEM_COLS = 512;
 // tensor-memory columns: S and O of tile A, then of tile B
 __device__ __forceinline__ uint32_t tm_s(int x) { return x ? 256u : 0u; }
@@ -164,6 +164,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int box_rows = bs < BN ? bs : BN;
   const int nbox = BN / box_rows;
 
+  // Registers: the block is launched with 384 x 168; the control warpgroup
+  // (producer, MMA issuer, two idle warps) keeps 120 per thread and the two
+  // softmax warpgroups take 184 (128 x 120 + 256 x 184 = 62,464 <= 64,512),
+  // enough to hold a whole S row per thread.
+
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ------
     // Fill order per item: K_0, V_0, K_1, V_1, ...  Lane i owns box i of a
@@ -336,12 +343,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     // drain: every MMA issued above has completed before TMEM is freed
     tc5::mma_commit(bar(B_FINAL));
     tc5::mbar_wait(bar(B_FINAL), 0, abort_flag, p.err, /*honor_abort=*/false);
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
     // ------------------------------------------------ softmax -----------
-    const int r = threadIdx.x - 128;               // query row of a tile
+    // Warps 4..7 own query tile A, warps 8..11 tile B; one thread per row.
+    const int x = (warp - 4) >> 2;                 // query tile of this warp
+    const int r = (threadIdx.x - 128) & 127;       // its row of the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_off + tm_s(x), to = tmem + lane_off + tm_o(x);
     const float scale_log2 = p.softmax_scale * kLog2e;
-    uint32_t sc[2] = {0, 0};  // S tiles seen per query tile
+    uint32_t sc = 0;  // S tiles seen
     uint32_t items = 0, fbase = 0;
     // waits whose outcome is the same for the whole warp, so that the warp
     // stays converged for the warp-collective tensor-memory accesses
@@ -353,55 +365,59 @@ __global__ void __launch_bounds__(THREADS, 1)
       Item it;
       if (!get_item(p, TQ, idx, it)) break;
       const int tr = r / G, hr = r % G;
-      bool valid[2];
-      int pos[2];
-      int64_t orow[2];
-      for (int x = 0; x < 2; ++x) {
-        valid[x] = tr < it.nq[x];
-        pos[x] = it.minpos[x] + tr;
-        orow[x] = (static_cast<int64_t>(it.q0[x] + tr) * p.num_q_heads + it.g * G + hr) * DV;
-      }
+      const bool valid = tr < it.nq[x];
+      const int pos = it.minpos[x] + tr;
+      const int64_t orow =
+          (static_cast<int64_t>(it.q0[x] + tr) * p.num_q_heads + it.g * G + hr) * DV;
       if (it.ntiles == 0) {
-        for (int x = 0; x < 2; ++x)
-          if (valid[x]) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow[x]);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
 #pragma unroll
-            for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float m = -INFINITY, l = 0.f;
       bool ok = true;
-      // One softmax step of query tile x over key tile j: S_x -> P_x.
-      auto step = [&](const int x, const int j, float& m, float& l) -> bool {
+      for (int j = 0; j < it.ntiles && ok; ++j) {
         const int kbase = j * BN;
-        if (!wwait(bar(B_SFULL0 + x), sc[x] & 1u)) return false;
-        ++sc[x];
+        if (!wwait(bar(B_SFULL0 + x), sc & 1u)) {
+          ok = false;
+          break;
+        }
+        ++sc;
         tc5::tc_fence_after();
-        float s[BN];
+        const bool masked = !valid || kbase + BN - 1 > pos;
+        float sv[BN];
         {
           uint32_t v[BN / 32][32];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            tc5::tmem_ld_32x32b_x32(tmem + lane_off + tm_s(x) + 32 * c, v[c]);
+          for (int c = 0; c < BN / 32; ++c) tc5::tmem_ld_32x32b_x32(ts + 32 * c, v[c]);
           tc5::tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-            for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(v[c][k]);
+            for (int k = 0; k < 32; ++k) sv[32 * c + k] = __uint_as_float(v[c][k]);
         }
-        if (!valid[x] || kbase + BN - 1 > pos[x]) {
+        if (masked) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)
-            if (!valid[x] || kbase + c > pos[x]) s[c] = -INFINITY;
+            if (!valid || kbase + c > pos) sv[c] = -INFINITY;
         }
-        float mx = -INFINITY;
+        float mx;
+        {
+          float mc[8];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+          for (int k = 0; k < 8; ++k) mc[k] = sv[k];
+#pragma unroll
+          for (int c = 8; c < BN; ++c) mc[c & 7] = fmaxf(mc[c & 7], sv[c]);
+          mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
+                     fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+        }
         const float m_new = fmaxf(m, mx * scale_log2);
         // The rescale touches O with warp-collective tensor-memory loads and
-        // stores, so it is decided per warp; PV_x(j-1) has completed (the
-        // commit behind S_x(j) covers it).
+        // stores, so it is decided per warp; PV(j-1) has completed (the
+        // commit behind S(j) covers it).
         const bool need = j > 0 && m_new > m + kRescaleThreshold;
         if (j == 0) {
           m = m_new;
@@ -410,38 +426,40 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t v[32];
-            tc5::tmem_ld_32x32b_x32(tmem + lane_off + tm_o(x) + 32 * c, v);
+            tc5::tmem_ld_32x32b_x32(to + 32 * c, v);
             tc5::tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tc5::tmem_st_32x32b_x32(tmem + lane_off + tm_o(x) + 32 * c, v);
+            tc5::tmem_st_32x32b_x32(to + 32 * c, v);
           }
           l *= alpha;
           m = m_new;
         }
         const float base = m == -INFINITY ? 0.f : m;
-        // P (bf16) over the first 64 columns of S_x
+        // P (bf16) over the first 64 columns of S
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_exp2(fmaf(s[32 * c + 2 * k], scale_log2, -base));
-            const float p1 = fast_exp2(fmaf(s[32 * c + 2 * k + 1], scale_log2, -base));
-            l += p0 + p1;
+            const float p0 = fast_exp2(fmaf(sv[32 * c + 2 * k], scale_log2, -base));
+            const float p1 = fast_exp2(fmaf(sv[32 * c + 2 * k + 1], scale_log2, -base));
+            ls[k & 3] += p0 + p1;
             pk[k] = pack_bf16x2(p0, p1);
           }
-          tc5::tmem_st_32x32b_x16(tmem + lane_off + tm_s(x) + 16 * c, pk);
+          tc5::tmem_st_32x32b_x16(ts + 16 * c, pk);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tc5::tmem_wait_st();
         bool zeroed = false;
         if (x == 0 && kbase + BN > it.L) {
           // last tile: zero the V rows of keys past the sequence end
           const uint32_t vfill = fbase + 5u * j + 3u;
-          for (int h = 0; h < VSLABS; ++h) {
+          for (int h = 0; h < VSLABS && ok; ++h) {
             const uint32_t fi = vfill + h;
-            if (!wwait(bar(B_SLAB_FULL0 + fi % NSLAB), (fi / NSLAB) & 1u)) return false;
-            if (kbase + r >= it.L) {
+            ok = wwait(bar(B_SLAB_FULL0 + fi % NSLAB), (fi / NSLAB) & 1u);
+            if (ok && kbase + r >= it.L) {
               uint4* vrow =
                   reinterpret_cast<uint4*>(smem + RING_OFF + (fi % NSLAB) * SLAB + r * 128);
 #pragma unroll
@@ -450,46 +468,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           zeroed = true;
         }
+        if (!ok) break;
         if (zeroed) tc5::fence_proxy_async_smem();
         tc5::tc_fence_before();
         tc5::mbar_arrive(bar(B_PFULL0 + x));
-        return true;
-      };
-      // Epilogue of query tile x: O_x / l -> bf16.
-      auto finish = [&](const int x, const float l) -> bool {
-        if (!wwait(bar(B_ODONE0 + x), items & 1u)) return false;
-        tc5::tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4 packed[DV / 8];
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16 ----
+      if (!wwait(bar(B_ODONE0 + x), items & 1u)) break;
+      tc5::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t v[32];
-          tc5::tmem_ld_32x32b_x32(tmem + lane_off + tm_o(x) + 32 * c, v);
-          tc5::tmem_wait_ld();
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t v[32];
+        tc5::tmem_ld_32x32b_x32(to + 32 * c, v);
+        tc5::tmem_wait_ld();
+        if (valid) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            packed[4 * c + k] = make_uint4(
+            dst[4 * c + k] = make_uint4(
                 pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
                 pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
                 pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
                 pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
         }
-        tc5::tc_fence_before();
-        tc5::mbar_arrive(bar(B_OFREE0 + x));
-        if (valid[x]) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow[x]);
-#pragma unroll
-          for (int c = 0; c < DV / 8; ++c) dst[c] = packed[c];
-        }
-        return true;
-      };
-      for (int j = 0; j < it.ntiles && ok; ++j) {
-        ok = step(0, j, m0, l0);
-        if (ok) ok = step(1, j, m1, l1);
       }
-      if (ok) ok = finish(0, l0);
-      if (ok) ok = finish(1, l1);
-      if (!ok) break;
+      tc5::tc_fence_before();
+      tc5::mbar_arrive(bar(B_OFREE0 + x));
       fbase += 5u * static_cast<uint32_t>(it.ntiles);
       ++items;
     }
