@@ -14,8 +14,8 @@
 //  * Persistent CTAs, one per SM.  A work item is two 128-row query tiles of
 //    one KV head (tiles A and B); a tile is 128 / G consecutive tokens x the
 //    G query heads that share the KV head (GQA packing), so each K/V tile
-//    staged in shared memory serves 2 x 128 query rows.  Items are taken
-//    longest-first.
+//    staged in shared memory serves 2 x 128 query rows.  Items are numbered
+//    longest-first and dealt to the CTAs in alternating directions.
 //  * Warp roles: warp 0 issues TMA loads (the two Q tiles as 64-column slabs;
 //    K and V pages as 64-column boxes of one page each into 128-key slabs of
 //    an 8-slab ring; page ids prefetched two tiles ahead by all lanes),
@@ -26,7 +26,8 @@
 //    S_A(j) and S_B(j) = Q K_j^T (M 128, N 128, K 192, operands in shared
 //    memory); the softmax turns S_X(j) into bf16 P and stores it over S_X's
 //    first 64 columns in tensor memory; O_X += P V_j reads P straight from
-//    tensor memory (A operand) and V_j from shared memory (two N = 64 halves).
+//    tensor memory (A operand) and V_j from shared memory in one N = 128 MMA
+//    per 16 keys (an N = 64 MMA costs as much time as an N = 128 one).
 //    Issue order: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
 //    A commit after S_X(j+1) also covers PV_X(j), so when the softmax sees
 //    S_X(j+1) ready, P_X(j) has been consumed and O_X is stable.
@@ -82,6 +83,23 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+// Ring fills of an item: five per key tile (K's three slabs, V's two), tile j
+// taking fills fbase + 5j .. fbase + 5j + 4.  One N = 128 MMA reads both V
+// slabs at a fixed stride, so they must sit in adjacent slots; in the one
+// tile position in eight where they would straddle the end of the ring, the
+// tile's V is filled before its K.
+constexpr int FILLS_PER_TILE = KSLABS + VSLABS;
+static_assert(FILLS_PER_TILE == 5 && NSLAB == 8, "fill pattern");
+__device__ __forceinline__ bool v_first(uint32_t fbase, int j) {
+  return (fbase + FILLS_PER_TILE * j + KSLABS) % NSLAB == NSLAB - 1;
+}
+__device__ __forceinline__ uint32_t k_fill(uint32_t fbase, int j, int c) {
+  return fbase + FILLS_PER_TILE * j + (v_first(fbase, j) ? VSLABS : 0) + c;
+}
+__device__ __forceinline__ uint32_t v_fill(uint32_t fbase, int j, int h) {
+  return fbase + FILLS_PER_TILE * j + (v_first(fbase, j) ? 0 : KSLABS) + h;
+}
+
 struct Item {
   int b, g, L, qlen;
   int q0[2], nq[2], minpos[2];
@@ -120,6 +138,15 @@ __device__ __forceinline__ bool get_item(const AttnParams& p, int TQ, int idx,
     acc += cnt;
   }
   return false;
+}
+
+// The k-th item of this CTA.  Items are numbered longest-first and dealt in
+// rounds of gridDim.x, alternately forwards and backwards, so that every CTA's
+// total work is about the same.
+__device__ __forceinline__ int item_index(int k) {
+  const int r = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                        : static_cast<int>(blockIdx.x);
+  return k * static_cast<int>(gridDim.x) + r;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -214,9 +241,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       ++f;
       return true;
     };
-    for (int idx = blockIdx.x; ok; idx += gridDim.x) {
+    for (int k = 0; ok; ++k) {
       Item it;
-      if (!get_item(p, TQ, idx, it)) break;
+      if (!get_item(p, TQ, item_index(k), it)) break;
       if (it.ntiles == 0) continue;
       bt_row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
       int pid0 = load_pid(it, 0), pid1 = load_pid(it, 1);
@@ -235,8 +262,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       ++qi;
       for (int j = 0; j < it.ntiles && ok; ++j) {
         const int pid2 = load_pid(it, j + 2);  // prefetch
+        const bool vf = v_first(f, 0);
+        for (int h = 0; h < VSLABS && ok && vf; ++h) ok = fill_slab(it, j, p.v_off + 64 * h, pid0);
         for (int c = 0; c < KSLABS && ok; ++c) ok = fill_slab(it, j, p.k_off + 64 * c, pid0);
-        for (int h = 0; h < VSLABS && ok; ++h) ok = fill_slab(it, j, p.v_off + 64 * h, pid0);
+        for (int h = 0; h < VSLABS && ok && !vf; ++h) ok = fill_slab(it, j, p.v_off + 64 * h, pid0);
         pid0 = pid1;
         pid1 = pid2;
       }
@@ -254,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ MMA issuer --------
     constexpr uint32_t idesc_s = tc5::idesc_bf16_f32(BM, BN, false);
-    constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(BM, 64, true);
+    constexpr uint32_t idesc_pv = tc5::idesc_bf16_f32(BM, DV, true);
     uint32_t qi = 0, fbase = 0;
     uint32_t pc[2] = {0, 0};  // P tiles consumed per query tile
     bool ok = true;
@@ -266,13 +295,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto wait_fill = [&](uint32_t fill) {
       return wait(B_SLAB_FULL0 + fill % NSLAB, (fill / NSLAB) & 1u);
     };
-    // S_x = Q_x K_j^T; K_j's three slabs are fills kf .. kf + 2
-    auto issue_s = [&](int x, uint32_t kf) {
+    // S_x = Q_x K_j^T
+    auto issue_s = [&](int x, uint32_t fb, int j) {
       tc5::tc_fence_after();
 #pragma unroll
       for (int c = 0; c < KSLABS; ++c) {
         const uint32_t qa = sbase + Q_OFF + (x * KSLABS + c) * SLAB;
-        const uint32_t ka = slab_addr(kf + c);
+        const uint32_t ka = slab_addr(k_fill(fb, j, c));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc5::mma_f16_ss(tmem + tm_s(x), tc5::sdesc_sw128(qa + 32 * kk, 16, 1024),
@@ -281,63 +310,58 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc5::mma_commit(bar(B_SFULL0 + x));
     };
-    // O_x += P_x V_j; V_j's two slabs are fills vf, vf + 1
-    auto issue_pv = [&](int x, uint32_t vf, bool first) {
+    // O_x += P_x V_j: N = 128 over V's two adjacent 64-column slabs (the
+    // leading byte offset steps from one to the other), K = 16 keys a step
+    auto issue_pv = [&](int x, uint32_t fb, int j, bool first) {
       tc5::tc_fence_after();
+      const uint32_t va = slab_addr(v_fill(fb, j, 0));
 #pragma unroll
-      for (int h = 0; h < VSLABS; ++h) {
-        const uint32_t va = slab_addr(vf + h);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          tc5::mma_f16_ts(tmem + tm_o(x) + 64 * h, tmem + tm_s(x) + 8 * kk,
-                          tc5::sdesc_sw128(va + kk * 2048, SLAB, 1024), idesc_pv,
-                          (!first || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < BN / 16; ++kk)
+        tc5::mma_f16_ts(tmem + tm_o(x), tmem + tm_s(x) + 8 * kk,
+                        tc5::sdesc_sw128(va + kk * 2048, SLAB, 1024), idesc_pv,
+                        (!first || kk > 0) ? 1u : 0u);
     };
-    for (int idx = blockIdx.x; ok; idx += gridDim.x) {
+    for (int k = 0; ok; ++k) {
       Item it;
-      if (!get_item(p, TQ, idx, it)) break;
+      if (!get_item(p, TQ, item_index(k), it)) break;
       if (it.ntiles == 0) continue;
       const int n = it.ntiles;
       if (!wait(B_QFULL, qi & 1u)) break;
       // S_A(0), S_B(0)
-      for (int c = 0; c < KSLABS; ++c) wait_fill(fbase + c);
+      for (int c = 0; c < KSLABS; ++c) wait_fill(k_fill(fbase, 0, c));
       if (!ok) break;
-      issue_s(0, fbase);
-      issue_s(1, fbase);
+      issue_s(0, fbase, 0);
+      issue_s(1, fbase, 0);
       if (n == 1) tc5::mma_commit(bar(B_QEMPTY));
-      for (int c = 0; c < KSLABS; ++c) tc5::mma_commit(bar(B_SLAB_EMPTY0 + (fbase + c) % NSLAB));
+      for (int c = 0; c < KSLABS; ++c)
+        tc5::mma_commit(bar(B_SLAB_EMPTY0 + k_fill(fbase, 0, c) % NSLAB));
       for (int j = 0; j < n && ok; ++j) {
-        const uint32_t vf = fbase + 5 * j + 3;       // V_j
-        const uint32_t kf = fbase + 5 * (j + 1);     // K_{j+1}
         for (int x = 0; x < 2 && ok; ++x) {
-          if (x == 0) {
-            wait_fill(vf);
-            wait_fill(vf + 1);
-          }
+          if (x == 0)
+            for (int h = 0; h < VSLABS; ++h) wait_fill(v_fill(fbase, j, h));
           wait(B_PFULL0 + x, pc[x] & 1u);
           if (j == 0) wait(B_OFREE0 + x, (qi & 1u) ^ 1u);
           if (!ok) break;
           ++pc[x];
-          issue_pv(x, vf, j == 0);
+          issue_pv(x, fbase, j, j == 0);
           if (j == n - 1) tc5::mma_commit(bar(B_ODONE0 + x));
           if (x == 1)
             for (int h = 0; h < VSLABS; ++h)
-              tc5::mma_commit(bar(B_SLAB_EMPTY0 + (vf + h) % NSLAB));
+              tc5::mma_commit(bar(B_SLAB_EMPTY0 + v_fill(fbase, j, h) % NSLAB));
           if (j + 1 < n) {
             if (x == 0)
-              for (int c = 0; c < KSLABS; ++c) wait_fill(kf + c);
+              for (int c = 0; c < KSLABS; ++c) wait_fill(k_fill(fbase, j + 1, c));
             if (!ok) break;
-            issue_s(x, kf);
+            issue_s(x, fbase, j + 1);
             if (x == 1) {
               if (j + 2 == n) tc5::mma_commit(bar(B_QEMPTY));  // last S issued
               for (int c = 0; c < KSLABS; ++c)
-                tc5::mma_commit(bar(B_SLAB_EMPTY0 + (kf + c) % NSLAB));
+                tc5::mma_commit(bar(B_SLAB_EMPTY0 + k_fill(fbase, j + 1, c) % NSLAB));
             }
           }
         }
       }
-      fbase += 5u * static_cast<uint32_t>(n);
+      fbase += FILLS_PER_TILE * static_cast<uint32_t>(n);
       ++qi;
     }
     // drain: every MMA issued above has completed before TMEM is freed
@@ -361,9 +385,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool rr = tc5::mbar_wait(b, parity, abort_flag, p.err);
       return __all_sync(0xffffffffu, rr);
     };
-    for (int idx = blockIdx.x;; idx += gridDim.x) {
+    for (int k = 0;; ++k) {
       Item it;
-      if (!get_item(p, TQ, idx, it)) break;
+      if (!get_item(p, TQ, item_index(k), it)) break;
       const int tr = r / G, hr = r % G;
       const bool valid = tr < it.nq[x];
       const int pos = it.minpos[x] + tr;
@@ -455,9 +479,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool zeroed = false;
         if (x == 0 && kbase + BN > it.L) {
           // last tile: zero the V rows of keys past the sequence end
-          const uint32_t vfill = fbase + 5u * j + 3u;
           for (int h = 0; h < VSLABS && ok; ++h) {
-            const uint32_t fi = vfill + h;
+            const uint32_t fi = v_fill(fbase, j, h);
             ok = wwait(bar(B_SLAB_FULL0 + fi % NSLAB), (fi / NSLAB) & 1u);
             if (ok && kbase + r >= it.L) {
               uint4* vrow =
@@ -496,7 +519,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc5::tc_fence_before();
       tc5::mbar_arrive(bar(B_OFREE0 + x));
-      fbase += 5u * static_cast<uint32_t>(it.ntiles);
+      fbase += FILLS_PER_TILE * static_cast<uint32_t>(it.ntiles);
       ++items;
     }
   }
