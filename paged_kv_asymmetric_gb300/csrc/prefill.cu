@@ -11,14 +11,20 @@
 //
 // GB300 design (prior art on the pages was an sm_120 mma.sync kernel; this is
 // not a translation of it):
-//  * Persistent CTAs, one per SM.  A work item is two 128-row query tiles of
-//    one KV head (tiles A and B); a tile is 128 / G consecutive tokens x the
-//    G query heads that share the KV head (GQA packing), so each K/V tile
-//    staged in shared memory serves 2 x 128 query rows.  Items are numbered
-//    longest-first and dealt to the CTAs in alternating directions.
+//  * Persistent clusters of two CTAs, one CTA per SM.  A CTA's work item is
+//    two 128-row query tiles of one KV head (tiles A and B); a tile is 128 / G
+//    consecutive tokens x the G query heads that share the KV head (GQA
+//    packing).  The two CTAs of a cluster take adjacent items of the same
+//    sequence and KV head and walk the same key tiles: each K/V box is read
+//    from L2 once, by one of them, and multicast into both shared memories,
+//    so a K/V tile feeds 4 x 128 query rows.  (Without this the loads alone
+//    ran at ~3.6 TB/s from L2 and bounded the kernel.)  Units are numbered
+//    longest-first and dealt to the clusters in alternating directions.
 //  * Warp roles: warp 0 issues TMA loads (the two Q tiles as 64-column slabs;
 //    K and V pages as 64-column boxes of one page each into 128-key slabs of
-//    an 8-slab ring; page ids prefetched two tiles ahead by all lanes),
+//    an 8-slab ring, half of each slab's boxes per CTA; a slot is refilled
+//    once the MMAs of both CTAs have read it; page ids prefetched two tiles
+//    ahead by all lanes),
 //    warp 1 issues tcgen05.mma from one thread, warps 4..7 run the softmax
 //    of tile A and warps 8..11 that of tile B, one thread per query row.
 //  * Tensor memory holds S and O of both tiles (4 x 128 columns).  The
@@ -106,32 +112,39 @@ struct Item {
   int nkeys, ntiles;
 };
 
-// The idx-th work item: query tiles 2i and 2i+1 of one sequence and KV
-// head, longest-first within each sequence; false when idx is past the end.
-__device__ __forceinline__ bool get_item(const AttnParams& p, int TQ, int idx,
-                                         Item& it) {
+constexpr int CLUSTER = 2;          // CTAs sharing each K/V load
+constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
+
+// The idx-th work unit, as seen by cluster rank `rank`.  A unit is query
+// tiles 4u .. 4u + 3 of one sequence and KV head; rank r takes tiles 4u + 2r
+// and 4u + 2r + 1 (its item), and both ranks walk the key tiles of the unit's
+// last token, so that every K/V tile is loaded once for the pair (keys past a
+// row's position are masked as usual).  Units are numbered longest-first
+// within each sequence; false when idx is past the end.
+__device__ __forceinline__ bool get_unit(const AttnParams& p, int TQ, int idx,
+                                         int rank, Item& it) {
   int acc = 0;
   for (int b = 0; b < p.num_seqs; ++b) {
     const int qs = __ldg(p.query_start_loc + b);
     const int qlen = __ldg(p.query_start_loc + b + 1) - qs;
     const int ntq = (qlen + TQ - 1) / TQ;
-    const int npair = (ntq + 1) / 2;
-    const int cnt = npair * p.num_kv_heads;
+    const int nu = (ntq + 2 * CLUSTER - 1) / (2 * CLUSTER);
+    const int cnt = nu * p.num_kv_heads;
     if (idx < acc + cnt) {
       const int j = idx - acc;
-      const int pi = npair - 1 - j / p.num_kv_heads;
+      const int u = nu - 1 - j / p.num_kv_heads;
       it.b = b;
       it.g = j % p.num_kv_heads;
       it.L = __ldg(p.seq_lens + b);
       it.qlen = qlen;
       for (int x = 0; x < 2; ++x) {
-        const int t0 = (2 * pi + x) * TQ;
+        const int t0 = (2 * CLUSTER * u + 2 * rank + x) * TQ;
         it.q0[x] = qs + t0;
         it.nq[x] = max(0, min(TQ, qlen - t0));
         it.minpos[x] = it.L - qlen + t0;
       }
-      const int maxpos = it.minpos[0] + it.nq[0] + it.nq[1] - 1;
-      it.nkeys = max(0, min(maxpos + 1, it.L));
+      const int tend = min(qlen, 2 * CLUSTER * (u + 1) * TQ);  // past the unit's last token
+      it.nkeys = max(0, min(it.L - qlen + tend, it.L));
       it.ntiles = (it.nkeys + BN - 1) / BN;
       return true;
     }
@@ -140,13 +153,13 @@ __device__ __forceinline__ bool get_item(const AttnParams& p, int TQ, int idx,
   return false;
 }
 
-// The k-th item of this CTA.  Items are numbered longest-first and dealt in
-// rounds of gridDim.x, alternately forwards and backwards, so that every CTA's
-// total work is about the same.
-__device__ __forceinline__ int item_index(int k) {
-  const int r = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                        : static_cast<int>(blockIdx.x);
-  return k * static_cast<int>(gridDim.x) + r;
+// The k-th unit of this cluster.  Units are numbered longest-first and dealt
+// in rounds over the clusters, alternately forwards and backwards, so that
+// every cluster's total work is about the same.
+__device__ __forceinline__ int unit_index(int k) {
+  const int ncl = static_cast<int>(tc5::num_clusters_x());
+  const int cid = static_cast<int>(tc5::cluster_id_x());
+  return k * ncl + ((k & 1) ? ncl - 1 - cid : cid);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -163,6 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(tc5::cluster_ctarank());
   const int G = p.group;
   const int TQ = BM / G;
 
@@ -171,6 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t count = 1;
       if ((i >= B_PFULL0 && i < B_PFULL0 + 2) || (i >= B_OFREE0 && i < B_OFREE0 + 2))
         count = 128;
+      if (i >= B_SLAB_EMPTY0 && i < B_SLAB_EMPTY0 + NSLAB) count = CLUSTER;  // one per CTA
       tc5::mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -184,6 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc5::tc_fence_before();
   __syncthreads();
+  // the peer's barriers are initialised before either CTA's first copy
+  tc5::cluster_sync();
   tc5::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -224,7 +241,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0)
         tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * 128));
       __syncwarp();
-      if (lane < nb) {
+      // each box is copied by one rank into both CTAs (ranks alternate)
+      if (lane < nb && ((lane + static_cast<int>(f)) % CLUSTER) == rank) {
         const int key0 = kt * BN + lane * box_rows;
         const int off = key0 % bs;
         int page = pid;
@@ -234,16 +252,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t dst = sbase + RING_OFF + slot * SLAB + lane * box_rows * 128;
         if (p.layout == PKV_NHD)
-          tc5::tma_load_4d(dst, &kv_map, col, it.g, off, page, full);
+          tc5::tma_load_4d_mc(dst, &kv_map, col, it.g, off, page, full, CLUSTER_MASK);
         else
-          tc5::tma_load_4d(dst, &kv_map, col, off, it.g, page, full);
+          tc5::tma_load_4d_mc(dst, &kv_map, col, off, it.g, page, full, CLUSTER_MASK);
       }
       ++f;
       return true;
     };
     for (int k = 0; ok; ++k) {
       Item it;
-      if (!get_item(p, TQ, item_index(k), it)) break;
+      if (!get_unit(p, TQ, unit_index(k), rank, it)) break;
       if (it.ntiles == 0) continue;
       bt_row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks_per_seq;
       int pid0 = load_pid(it, 0), pid1 = load_pid(it, 1);
@@ -292,6 +310,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       return ok;
     };
     auto slab_addr = [&](uint32_t fill) { return sbase + RING_OFF + (fill % NSLAB) * SLAB; };
+    // a slot is free again once both CTAs' MMAs have read it
+    auto release = [&](uint32_t slot) {
+      tc5::mma_commit_mc(bar(B_SLAB_EMPTY0 + slot), CLUSTER_MASK);
+    };
     auto wait_fill = [&](uint32_t fill) {
       return wait(B_SLAB_FULL0 + fill % NSLAB, (fill / NSLAB) & 1u);
     };
@@ -323,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     for (int k = 0; ok; ++k) {
       Item it;
-      if (!get_item(p, TQ, item_index(k), it)) break;
+      if (!get_unit(p, TQ, unit_index(k), rank, it)) break;
       if (it.ntiles == 0) continue;
       const int n = it.ntiles;
       if (!wait(B_QFULL, qi & 1u)) break;
@@ -334,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       issue_s(1, fbase, 0);
       if (n == 1) tc5::mma_commit(bar(B_QEMPTY));
       for (int c = 0; c < KSLABS; ++c)
-        tc5::mma_commit(bar(B_SLAB_EMPTY0 + k_fill(fbase, 0, c) % NSLAB));
+        release(k_fill(fbase, 0, c) % NSLAB);
       for (int j = 0; j < n && ok; ++j) {
         for (int x = 0; x < 2 && ok; ++x) {
           if (x == 0)
@@ -347,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j == n - 1) tc5::mma_commit(bar(B_ODONE0 + x));
           if (x == 1)
             for (int h = 0; h < VSLABS; ++h)
-              tc5::mma_commit(bar(B_SLAB_EMPTY0 + v_fill(fbase, j, h) % NSLAB));
+              release(v_fill(fbase, j, h) % NSLAB);
           if (j + 1 < n) {
             if (x == 0)
               for (int c = 0; c < KSLABS; ++c) wait_fill(k_fill(fbase, j + 1, c));
@@ -356,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (x == 1) {
               if (j + 2 == n) tc5::mma_commit(bar(B_QEMPTY));  // last S issued
               for (int c = 0; c < KSLABS; ++c)
-                tc5::mma_commit(bar(B_SLAB_EMPTY0 + k_fill(fbase, j + 1, c) % NSLAB));
+                release(k_fill(fbase, j + 1, c) % NSLAB);
             }
           }
         }
@@ -387,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     for (int k = 0;; ++k) {
       Item it;
-      if (!get_item(p, TQ, item_index(k), it)) break;
+      if (!get_unit(p, TQ, unit_index(k), rank, it)) break;
       const int tr = r / G, hr = r % G;
       const bool valid = tr < it.nq[x];
       const int pos = it.minpos[x] + tr;
@@ -531,6 +553,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc5::tc_fence_after();
     tc5::tmem_dealloc(tmem, TMEM_COLS);
   }
+  // Neither CTA leaves while the other may still signal its barriers (the
+  // MMA commits that free ring slots arrive in both CTAs).
+  tc5::cluster_sync();
 }
 
 }  // namespace
@@ -571,7 +596,34 @@ cudaError_t launch_prefill(const AttnParams& p, int num_sms,
   static int attr_set[64] = {0};
   cudaError_t e = ensure_smem_attr(prefill_kernel, SMEM_BYTES, attr_set);
   if (e != cudaSuccess) return e;
-  prefill_kernel<<<num_sms, THREADS, SMEM_BYTES, stream>>>(q_map, kv_map, p);
+  // Persistent: as many CTA pairs (clusters) as can be resident at once.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CLUSTER * CLUSTER));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int max_clusters[64] = {0};
+  int ncl = dev < 64 ? max_clusters[dev] : 0;
+  if (ncl == 0) {
+    e = cudaOccupancyMaxActiveClusters(&ncl, prefill_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (ncl < 1) return cudaErrorNotSupported;
+    if (dev < 64) max_clusters[dev] = ncl;
+  }
+  if (ncl > num_sms / CLUSTER) ncl = num_sms / CLUSTER;
+  cfg.gridDim = dim3(static_cast<unsigned>(ncl * CLUSTER));
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, kv_map, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -97,6 +97,50 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same tile into the shared memory of every CTA of the cluster named in
+// `cta_mask`, at the same offset, each copy signalling the mbarrier at `bar`'s
+// offset in its own CTA.
+__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* map,
+                                               int c0, int c1, int c2, int c3,
+                                               uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], "
+      "%7;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------- clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;\n" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;\n" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster; orders this CTA's earlier memory
+// operations (mbarrier initialisation included) before the peers' later ones.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;\n" ::
+          : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map))
                : "memory");
@@ -178,6 +222,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];\n" ::"r"(bar)
+      : "memory");
+}
+
+// The same, arriving on the mbarrier at `bar`'s offset in every CTA of the
+// cluster named in `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "multicast::cluster.b64 [%0], %1;\n" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
