@@ -25,11 +25,12 @@
 //  * Consumer warps form NG groups of WG warps; chunk c (counted across
 //    units) goes to group c % NG, and the ring has a multiple of NG slots, so
 //    each slot is consumed by one group in order (no mbarrier phase can be
-//    mistaken for the one two fills later).  Within a group, warp w owns a slice of the K dimension
-//    for Q.K^T (partial scores summed through shared memory when WG > 1) and
-//    a slice of V's columns for P.V.  16 rows are below tcgen05's M = 64, and
-//    the FP8 operands are converted in registers, so the contraction runs on
-//    the warp-level m16n8k16 MMA (~4-32 flop per byte here).
+//    mistaken for the one two fills later).  Within a group, warp w owns a
+//    slice of the K dimension for Q.K^T (partial scores summed through
+//    shared memory when WG > 1) and a slice of V's columns for P.V.  16
+//    rows are below tcgen05's M = 64, and the FP8 operands are converted in
+//    registers, so the contraction runs on the warp-level m16n8k16 MMA
+//    (~4-32 flop per byte here).
 //  * bf16 cache: K and V fragments come from ldmatrix (.trans for V) on the
 //    swizzled slot.  fp8 cache: E4M3 codes become f16 in registers (exact),
 //    K through 16-byte loads with the reduction index permuted identically

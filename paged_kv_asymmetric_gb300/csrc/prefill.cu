@@ -531,12 +531,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc5::tmem_wait_ld();
         if (valid) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[4 * c + k] = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv),
-                pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv));
+          for (int k = 0; k < 4; ++k) {
+            auto o2 = [&](int i) {
+              return pack_bf16x2(__uint_as_float(v[8 * k + i]) * inv,
+                                 __uint_as_float(v[8 * k + i + 1]) * inv);
+            };
+            dst[4 * c + k] = make_uint4(o2(0), o2(2), o2(4), o2(6));
+          }
         }
       }
       tc5::tc_fence_before();
