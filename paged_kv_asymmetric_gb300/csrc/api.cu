@@ -261,6 +261,10 @@ int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
   const int64_t row_groups = (static_cast<int64_t>(max_query_len) * G + 15) / 16;
   if (row_groups * d->num_kv_heads > 65535 || num_seqs > 65535)
     return PKV_EINVAL;
+  // work units (split x sequence x KV head x row group) are counted in int
+  if (static_cast<int64_t>(num_splits) * num_seqs * d->num_kv_heads * row_groups >
+      (int64_t{1} << 30))
+    return PKV_EINVAL;
   // 16-key chunks are whole TMA boxes of one page (or two pages of 8)
   if (!(d->block_size % 16 == 0 || d->block_size == 8)) return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
@@ -311,9 +315,12 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
   int rc = device_info(nullptr, &sms);
   if (rc != PKV_OK) return rc;
   const int64_t G = num_q_heads / num_kv_heads;
-  const int64_t ctas = static_cast<int64_t>(num_seqs) * num_kv_heads *
-                       ((max_query_len * G + 15) / 16);
-  int64_t s = (2 * static_cast<int64_t>(sms) + ctas - 1) / ctas;
+  // work units per split: the decode kernel takes KV heads four at a time
+  // when the head count allows
+  const int64_t head_units = num_kv_heads % 4 == 0 ? num_kv_heads / 4 : num_kv_heads;
+  const int64_t units = static_cast<int64_t>(num_seqs) * head_units *
+                        ((max_query_len * G + 15) / 16);
+  int64_t s = (4 * static_cast<int64_t>(sms) + units - 1) / units;
   const int64_t pages = (static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size;
   if (s > pages) s = pages;
   if (s < 1) s = 1;

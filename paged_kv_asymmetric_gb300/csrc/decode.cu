@@ -11,26 +11,30 @@
 // GB300 design.  The path is bound by HBM bandwidth: every key's packed
 // K|V row is read once per (sequence, KV head) and serves all q_len * G query
 // rows of that KV head (G = Hq / Hkv).
-//  * Work unit = (split, sequence, KV head, 16-row group); the rows are
-//    (query token, query head) pairs, so a 1+3-token verify with G = 4 is one
-//    m16 tile.  Persistent CTAs (one per SM) take units round-robin and keep
-//    streaming across unit boundaries: loads for the next unit overlap the
-//    end of the current one, and no CTA pays a cold start per unit.
-//  * Warp 0 is the producer: it copies the unit's 16 query rows into a
-//    double-buffered Q slot (cp.async, completion on an mbarrier) and each
-//    16-key chunk of K|V rows into a ring slot with TMA boxes of 16 slots x
-//    128 bytes of one page and KV head (one instruction per box, 128-byte
-//    swizzle, columns past the row read as zero), page ids prefetched by all
-//    lanes ahead of use.
-//  * Consumer warps form NG groups of WG warps; chunk c (counted across
-//    units) goes to group c % NG, and the ring has a multiple of NG slots, so
-//    each slot is consumed by one group in order (no mbarrier phase can be
-//    mistaken for the one two fills later).  Within a group, warp w owns a
-//    slice of the K dimension for Q.K^T (partial scores summed through
-//    shared memory when WG > 1) and a slice of V's columns for P.V.  16
-//    rows are below tcgen05's M = 64, and the FP8 operands are converted in
-//    registers, so the contraction runs on the warp-level m16n8k16 MMA
-//    (~4-32 flop per byte here).
+//  * Work unit = (split, sequence, block of HPC KV heads, 16-row group); a
+//    row is a (query token, query head) pair of one KV head, so a 1+3-token
+//    verify with G = 4 is one m16 tile per head.  Persistent CTAs (one per
+//    SM) take units in alternating directions and keep streaming across unit
+//    boundaries.
+//  * Warp 0 is the producer: it stages each unit's query rows (cp.async,
+//    completion on an mbarrier), page ids and a descriptor ahead of use, and
+//    streams chunks of KPC keys x HPC heads into a ring with TMA boxes of up
+//    to KPC rows x 128 bytes of one page and head (128-byte swizzle, columns
+//    past the row read as zero), the boxes of a chunk issued by parallel
+//    lanes.  Measured on GB300, the rate at which one SM can bring in pages
+//    is set by the number of boxes and of chunk handshakes per byte, not by
+//    DRAM: 10 KB chunks (16 keys of one head) top out near 3.1 TB/s, 40 KB
+//    chunks (16 keys of four heads, or 64 keys of one) reach 6.6-7.3 TB/s.
+//    So a chunk holds four heads where Hkv allows, or more keys per head.
+//  * Consumer warps form groups of WG warps: group (h, n) handles head h of
+//    the block in every chunk c with c % NG == n.  The ring has a multiple
+//    of NG slots, so a slot is only consumed by the groups of one n, in fill
+//    order (no mbarrier phase can be mistaken for the one two fills later).
+//    Within a group, warp w owns a slice of the K dimension for Q.K^T
+//    (partial scores summed through shared memory when WG > 1) and a slice
+//    of V's columns for P.V.  16 rows are below tcgen05's M = 64, and the
+//    FP8 operands are converted in registers, so the contraction runs on the
+//    warp-level m16n8k16 MMA (~4-32 flop per byte here).
 //  * bf16 cache: K and V fragments come from ldmatrix (.trans for V) on the
 //    swizzled slot.  fp8 cache: E4M3 codes become f16 in registers (exact),
 //    K through 16-byte loads with the reduction index permuted identically
@@ -40,7 +44,8 @@
 //  * Online softmax in registers with exp2.  The last chunk of a unit has its
 //    rows past the last visible key zeroed in shared memory, so garbage in a
 //    partly filled page cannot reach the MMA; the scores of those keys are
-//    masked.  Groups merge (max, sum, O) through shared memory per unit.
+//    masked.  When NG > 1 the groups of a head combine (max, sum, O) in
+//    registers through shared memory at the end of a unit.
 //  * Every mbarrier wait is bounded; after a timeout the kernel records
 //    PKV_EDEV_TIMEOUT, the waits of all roles return at once, every warp
 //    still walks the same units (so named barriers stay matched), and the
@@ -56,22 +61,32 @@ namespace pkv {
 
 namespace {
 
-template <int DK_, int DV_, bool FP8_, int WG_, int NG_, int NSLOT_, int NQ_,
-          int SPAN_>
+template <int DK_, int DV_, bool FP8_, int HPC_, int WG_, int NG_, int KPC_,
+          int NSLOT_, int NQ_, int SPAN_, bool NARROW_ = false>
 struct DecodeCfg {
-  static constexpr int DK = DK_, DV = DV_, WG = WG_, NG = NG_;
-  static constexpr int NSLOT = NSLOT_, NQ = NQ_, SPAN = SPAN_;
+  static constexpr int DK = DK_, DV = DV_, HPC = HPC_, WG = WG_, NG = NG_;
+  static constexpr int KPC = KPC_, NSLOT = NSLOT_, NQ = NQ_, SPAN = SPAN_;
+  // narrow: a head's rows fit in 8 and the MMAs run transposed (S^T = K Q^T)
+  static constexpr bool NARROW = NARROW_;
+  static constexpr int QROWS = NARROW ? 8 : 16;           // staged Q rows per head
   static constexpr int MAXP = 128;  // page ids staged with a unit
   static constexpr bool FP8 = FP8_;
   static constexpr int ESZ = FP8 ? 1 : 2;
   static constexpr int SPAN_BYTES = SPAN * ESZ;
   static constexpr int NBOX = (SPAN_BYTES + 127) / 128;  // 128-byte column boxes
   static constexpr int BOX_COLS = 128 / ESZ;
-  static constexpr int SLOT_BYTES = NBOX * 16 * 128;
-  static constexpr int NCW = WG * NG;                      // consumer warps
+  // A ring slot is [column box][head][KPC rows][128 bytes]: one head's rows
+  // of a 128-byte column slice are contiguous (CB_BYTES), the HPC heads of a
+  // slice are adjacent (CB_STRIDE) so that one TMA box can bring them all.
+  static constexpr int CB_BYTES = KPC * 128;
+  static constexpr int CB_STRIDE = HPC * CB_BYTES;
+  static constexpr int SLOT_BYTES = NBOX * CB_STRIDE;
+  static constexpr int NGRP = HPC * NG;                  // consumer groups
+  static constexpr int NCW = NGRP * WG;                  // consumer warps
   static constexpr int THREADS = 32 * (1 + NCW);
-  static constexpr int QCH = DK * 2 / 16;                  // 16-byte Q pieces per row
-  static constexpr int Q_BYTES = 16 * DK * 2;
+  static constexpr int QCH = DK * 2 / 16;                // 16-byte Q pieces per row
+  static constexpr int QH_BYTES = QROWS * DK * 2;        // one head's Q rows
+  static constexpr int Q_BYTES = HPC * QH_BYTES;
   static constexpr int KSTEPS = DK / 16;
   static constexpr int KSW = KSTEPS / WG;                  // bf16: k-steps per warp
   static constexpr int NU = DK / 64;                       // fp8: 64-wide units
@@ -83,25 +98,45 @@ struct DecodeCfg {
   static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
   static constexpr int DESC_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int DESC_BYTES = 64 + MAXP * 4;  // descriptor + page ids
-  static constexpr int MERGE_OFF = DESC_OFF + NQ * DESC_BYTES;
-  static constexpr int MERGE = NG > 1 ? NG * 16 * DVP * 4 + 2 * NG * 16 * 4 : 0;
+  static constexpr int MAXSORT = 128;  // sequences ranked by length, at most
+  static constexpr int ORDER_OFF = DESC_OFF + NQ * DESC_BYTES;
+  static constexpr int MERGE_OFF = ORDER_OFF + MAXSORT * 4;
+  // every chunk class's (O, max, sum) per head and row, combined by all
+  static constexpr int MROW = DVP + 2;
+  static constexpr int MERGE = NG > 1 ? NG * HPC * 16 * MROW * 4 : 0;
   static constexpr int SBUF_OFF = MERGE_OFF + MERGE;
-  static constexpr int SBUF = WG > 1 ? NG * 2 * WG * 32 * 8 * 4 : 0;
+  static constexpr int SBUF_LANE = NARROW ? 4 : 8;  // partial scores per lane
+  static constexpr int SBUF = WG > 1 ? NGRP * 2 * WG * 32 * SBUF_LANE * 4 : 0;
   static constexpr int BAR_OFF = SBUF_OFF + SBUF;
   static constexpr int NBAR = 2 * NSLOT + 2 * NQ;
   static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
   static_assert(DK % 64 == 0 && KSTEPS % WG == 0, "K slices");
   static_assert(DV % WG == 0 && DVS % (FP8 ? 128 : 16) == 0, "V slices");
   static_assert(QCH % 8 == 0, "Q rows in whole 128-byte groups");
+  static_assert(KPC % 16 == 0 && KPC <= 256, "keys per chunk");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  static_assert(NSLOT % NG == 0, "each ring slot belongs to one consumer group");
+  static_assert(NSLOT % NG == 0, "each ring slot belongs to one chunk class");
+  static_assert(NGRP + 2 <= 15, "named barrier ids");
+  static_assert(!NARROW || (!FP8 && NG == 1 && KSW % 2 == 0 && DVS % 16 == 0),
+                "narrow form: bf16, one chunk class, k-step pairs, 16-column V tiles");
 };
 
 // Address of the 16-byte piece `piece` (byte offset / 16 within the staged
-// span) of key row `row` in a ring slot: TMA box piece/8 holds 16 rows x 128
-// bytes, and the 128-byte swizzle permutes 16-byte pieces by the row index.
-__device__ __forceinline__ uint32_t slot_piece(uint32_t slot, int row, int piece) {
-  return slot + (piece >> 3) * 2048 + row * 128 + (((piece & 7) ^ (row & 7)) << 4);
+// span) of key row `row` of one head's part of a ring slot (`sub` = the slot
+// + head * CB_BYTES): column slice piece/8 is CB_STRIDE further on, holding
+// the head's rows x 128 bytes, and the 128-byte swizzle permutes 16-byte
+// pieces by the row index.
+template <int CB_STRIDE>
+__device__ __forceinline__ uint32_t slot_piece(uint32_t sub, int row, int piece) {
+  return sub + (piece >> 3) * CB_STRIDE + row * 128 + (((piece & 7) ^ (row & 7)) << 4);
+}
+
+// Transposes an 8x8 matrix of 16-bit values held in the MMA fragment layout
+// (thread t: row t/4, columns 2(t%4) and 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // Q rows (bf16, DK wide) in a Q slot: rows of DK*2 bytes, 16-byte pieces
@@ -143,31 +178,41 @@ __device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
   return r != 0;
 }
 
+// Rows of one TMA box: the largest power of two <= kpc that divides the
+// block size, so that a chunk's boxes tile it and none straddles a page.
+__host__ __device__ constexpr int box_rows_for(int bs, int kpc) {
+  int r = kpc;
+  while (r > 1 && bs % r != 0) r >>= 1;
+  return r;
+}
+
 // A work unit; the producer stages it in shared memory as 16 ints followed
 // by its page ids.
 struct Unit {
-  int b, g, s, row0, nrows, qs, qlen, L;
+  int b, hb, s, row0, nrows, qs, qlen, L;
   int klo, khi, kmax, nch, page_lo, npages, pad0, pad1;
 };
 static_assert(sizeof(Unit) == 64, "descriptor size");
 
-// Sequence of unit u: split-major order over (split, sequence, KV head, row
-// group).
-__device__ __forceinline__ int unit_seq(const AttnParams& p, int RG, int u) {
-  const int per_split = p.num_seqs * p.num_kv_heads * RG;
-  return (u % per_split) / (p.num_kv_heads * RG);
-}
+// Units are numbered sequence-major, longest sequence first (when the
+// sequences were ranked), then over (split, row group, head block); the
+// CTAs take them in rounds, alternately forwards and backwards, so that
+// every CTA's share of keys is about the same.
+struct UnitShape {
+  int S, HB, RG;  // splits, head blocks per sequence, 16-row groups per head
+  __device__ int per_seq() const { return S * RG * HB; }
+};
 
-// Unit u's parameters from its sequence's query_start_loc pair and length.
-__device__ __forceinline__ void unit_params(const AttnParams& p, int RG, int u,
+// Unit u's parameters, for sequence b (the rank-u / per_seq sequence) with
+// its query_start_loc pair and length.
+template <int KPC>
+__device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, int u, int b,
                                             int q0, int q1, int L, Unit& un) {
-  const int per_split = p.num_seqs * p.num_kv_heads * RG;
-  un.s = u / per_split;
-  int rem = u - un.s * per_split;
-  un.b = rem / (p.num_kv_heads * RG);
-  rem -= un.b * p.num_kv_heads * RG;
-  un.g = rem % p.num_kv_heads;
-  const int rg = rem / p.num_kv_heads;
+  const int rem = u % us.per_seq();
+  un.b = b;
+  un.hb = rem % us.HB;
+  const int rg = (rem / us.HB) % us.RG;
+  un.s = rem / (us.HB * us.RG);
   const int G = p.group;
   un.qs = q0;
   un.qlen = q1 - q0;
@@ -187,7 +232,7 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, int RG, int u,
     const int i_last = (un.row0 + un.nrows - 1) / G;
     un.kmax = min(un.khi, max(0, min(un.L, un.L - un.qlen + i_last + 1)));
   }
-  un.nch = un.kmax > un.klo ? (un.kmax - un.klo + 15) / 16 : 0;
+  un.nch = un.kmax > un.klo ? (un.kmax - un.klo + KPC - 1) / KPC : 0;
   un.page_lo = page_lo;
   un.npages = page_hi - page_lo;
   un.pad0 = un.pad1 = 0;
@@ -195,10 +240,11 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, int RG, int u,
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p,
+                  int head_boxes) {
   extern __shared__ uint8_t smem_raw[];
   constexpr bool FP8 = C::FP8;
-  constexpr int WG = C::WG, NG = C::NG, NSLOT = C::NSLOT;
+  constexpr int HPC = C::HPC, WG = C::WG, NG = C::NG, KPC = C::KPC, NSLOT = C::NSLOT;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
@@ -218,18 +264,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int RG = (p.max_query_len * G + 15) / 16;
-  const int num_units = p.num_splits * p.num_seqs * p.num_kv_heads * RG;
+  const UnitShape us{p.num_splits, p.num_kv_heads / HPC, (p.max_query_len * G + 15) / 16};
+  const int num_units = p.num_seqs * us.per_seq();
   const int bs = p.block_size;
-  const int box_rows = bs < 16 ? bs : 16;
-  const int nrb = 16 / box_rows;  // row boxes per chunk
+  const int box_rows = box_rows_for(bs, KPC);
+  const int nrb = KPC / box_rows;  // row boxes per column box of a chunk
   const int lo = min(p.k_off, p.v_off);
   const int64_t T = p.num_tokens;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       tc5::mbar_init(slot_full(i), 1);
-      tc5::mbar_init(slot_empty(i), WG);
+      tc5::mbar_init(slot_empty(i), HPC * WG);  // every warp of one chunk class
     }
     for (int i = 0; i < C::NQ; ++i) {
       tc5::mbar_init(q_full(i), 1);
@@ -239,6 +285,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc5::fence_mbar_init();
     tc5::prefetch_tmap(&kv_map);
   }
+  // Q slots start as zeros: a unit stages only its valid rows, and the rows
+  // past them (masked, never written out) only need to be finite.
+  for (int i = threadIdx.x; i < C::NQ * C::Q_BYTES / 16; i += C::THREADS)
+    reinterpret_cast<uint4*>(smem + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   if (warp == 0) {
@@ -250,35 +300,77 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint32_t gc = 0;    // chunks issued
     uint32_t qs_n = 0;  // units staged
     uint32_t qi_n = 0;  // units issued
-    const int my_units =
-        static_cast<int>(blockIdx.x) < num_units
-            ? (num_units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-            : 0;
-    int pos = 0;                 // next position in this CTA's unit list
-    int mq0 = 0, mq1 = 0, mL = 0;  // metadata of the unit at `pos`
+    // the k-th unit of this CTA: rounds of gridDim.x units, dealt forwards
+    // and backwards in turn
+    auto unit_at = [&](int k) {
+      const int r = (k & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                            : static_cast<int>(blockIdx.x);
+      return k * static_cast<int>(gridDim.x) + r;
+    };
+    // Sequences ranked by decreasing length (ties by index) when there are
+    // few enough to rank here; otherwise in their own order.
+    int* order = reinterpret_cast<int*>(smem + C::ORDER_OFF);
+    const bool ranked = p.num_seqs <= C::MAXSORT;
+    if (ranked) {
+      // lane l holds the lengths of sequences l, l + 32, l + 64, l + 96 and
+      // counts, for each, the sequences that come before it
+      static_assert(C::MAXSORT == 128, "four sequences per lane");
+      const int nb = p.num_seqs, nu = (nb + 31) / 32;
+      int v[4], rank[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = lane + 32 * t;
+        v[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+        rank[t] = 0;
+      }
+      for (int u = 0; u < nu; ++u) {
+        const int vu = u == 0 ? v[0] : u == 1 ? v[1] : u == 2 ? v[2] : v[3];
+        for (int src = 0; src < 32; ++src) {
+          const int lj = __shfl_sync(0xffffffffu, vu, src);
+          const int j = src + 32 * u;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int i = lane + 32 * t;
+            rank[t] += (j < nb) && (lj > v[t] || (lj == v[t] && j < i));
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (lane + 32 * t < nb) order[rank[t]] = lane + 32 * t;
+      __syncwarp();
+    }
+    auto seq_of = [&](int u) {
+      const int r = u / us.per_seq();
+      return ranked ? order[r] : r;
+    };
+    int pos = 0;                   // next position in this CTA's unit list
+    int mb = 0, mq0 = 0, mq1 = 0, mL = 0;  // metadata of the unit at `pos`
     auto meta_load = [&](int ps) {
-      if (ps < my_units) {
-        const int b = unit_seq(p, RG, blockIdx.x + ps * gridDim.x);
-        mq0 = __ldg(p.query_start_loc + b);
-        mq1 = __ldg(p.query_start_loc + b + 1);
-        mL = __ldg(p.seq_lens + b);
+      const int u = unit_at(ps);
+      if (u < num_units) {
+        mb = seq_of(u);
+        mq0 = __ldg(p.query_start_loc + mb);
+        mq1 = __ldg(p.query_start_loc + mb + 1);
+        mL = __ldg(p.seq_lens + mb);
       }
     };
     meta_load(0);
     bool alive = true;
     auto stage_next = [&]() {
-      while (pos < my_units) {
+      while (unit_at(pos) < num_units) {
         Unit un;
-        unit_params(p, RG, blockIdx.x + pos * gridDim.x, mq0, mq1, mL, un);
+        unit_params<KPC>(p, us, unit_at(pos), mb, mq0, mq1, mL, un);
         ++pos;
         meta_load(pos);  // the next unit's metadata is in flight meanwhile
         if (un.nrows == 0) continue;
         if (un.nch == 0) {  // no key of this segment is visible to any row
-          for (int r = lane; r < un.nrows; r += 32) {
+          for (int i = lane; i < HPC * un.nrows; i += 32) {
+            const int h = i / un.nrows, r = i - h * un.nrows;
             const int rr = un.row0 + r;
             const int64_t t = un.qs + rr / G;
-            const int h = un.g * G + rr % G;
-            p.partial_lse[(un.s * T + t) * p.num_q_heads + h] = -INFINITY;
+            const int qh = (un.hb * HPC + h) * G + rr % G;
+            p.partial_lse[(un.s * T + t) * p.num_q_heads + qh] = -INFINITY;
           }
           continue;
         }
@@ -291,15 +383,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           return;
         }
         const uint32_t qdst = sbase + C::Q_OFF + qslot * C::Q_BYTES;
-        for (int i = lane; i < 16 * C::QCH; i += 32) {
-          const int r = i / C::QCH, j = i - r * C::QCH;
-          const bool valid = r < un.nrows;
+        const int qn = min(un.nrows, C::QROWS) * C::QCH;  // pieces of one head's valid rows
+        for (int i = lane; i < HPC * qn; i += 32) {
+          const int h = i / qn, rj = i - h * qn;
+          const int r = rj / C::QCH, j = rj - r * C::QCH;
           const int rr = un.row0 + r;
           const int64_t t = un.qs + rr / G;
-          const int h = un.g * G + rr % G;
-          const __nv_bfloat16* src =
-              valid ? p.q + (t * p.num_q_heads + h) * C::DK + j * 8 : p.q;
-          cp_async_16(q_piece<C::DK>(qdst, r, j), src, valid ? 16 : 0);
+          const int qh = (un.hb * HPC + h) * G + rr % G;
+          cp_async_16(q_piece<C::DK>(qdst + h * C::QH_BYTES, r, j),
+                      p.q + (t * p.num_q_heads + qh) * C::DK + j * 8, 16);
         }
         const int np = min(un.npages, C::MAXP);
         const int32_t* bt = p.block_table +
@@ -312,68 +404,64 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return;
       }
     };
+    // One unit is staged ahead: the next unit is staged while the ring is
+    // full of the current one's chunks, so unit boundaries cost no wait.
     stage_next();
-    if (alive) stage_next();
     while (alive && qi_n < qs_n) {
       const uint32_t qslot = qi_n % C::NQ;
-      // this unit's copies are complete once at most the newer unit's group
-      // is still pending
-      if (qs_n - qi_n >= 2)
-        cp_async_wait<1>();
-      else
-        cp_async_wait<0>();
+      cp_async_wait<0>();  // this unit's rows and page ids (staged last)
       __syncwarp();
       if (lane == 0) tc5::mbar_arrive(q_full(qslot));
       const Unit un = *desc_of(qslot);
       const int* pages = pages_of(qslot);
       const int32_t* bt = p.block_table + static_cast<int64_t>(un.b) * p.max_blocks_per_seq;
-      // Chunks go out in batches of PB: lane i owns chunk i of the batch
-      // (its slot wait, its transaction count, its page ids and its boxes),
-      // so the fixed cost of getting a chunk under way is paid in parallel.
-      constexpr int PB = C::NSLOT / 3 > 1 ? C::NSLOT / 3 : 1;
-      for (int k0 = 0; k0 < un.nch; k0 += PB) {
-        const int nbatch = min(PB, un.nch - k0);
-        const bool mine = lane < nbatch;
-        const uint32_t c = gc + lane;
-        const uint32_t slot = c % NSLOT;
+      const int k_stage = min(un.nch, NSLOT) - 1;  // stage the next unit after this chunk
+      for (int k = 0; k < un.nch; ++k) {
+        const uint32_t slot = gc % NSLOT;
         bool w = true;
-        if (mine)
-          w = tc5::mbar_wait(slot_empty(slot), ((c / NSLOT) & 1u) ^ 1u, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, w)) {
+        if (lane == 0)
+          w = tc5::mbar_wait(slot_empty(slot), ((gc / NSLOT) & 1u) ^ 1u, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
           alive = false;
           break;
         }
-        if (mine) {
-          const int kb = un.klo + (k0 + lane) * 16;
-          const int nvr = min(nrb, (un.kmax - kb + box_rows - 1) / box_rows);
+        // the chunk's boxes, issued by parallel lanes: with head boxes one
+        // per column slice (HPC heads x KPC rows), else one per head, column
+        // slice and row box that holds visible keys
+        const int kb = un.klo + k * KPC;
+        const int nvr = min(nrb, (un.kmax - kb + box_rows - 1) / box_rows);
+        const int per_head = C::NBOX * nvr;
+        if (lane == 0)
           tc5::mbar_arrive_expect_tx(slot_full(slot),
-                                     static_cast<uint32_t>(nvr * C::NBOX * box_rows * 128));
-          for (int rb = 0; rb < nvr; ++rb) {
-            const int key0 = kb + rb * box_rows;
-            const int pidx = key0 / bs - un.page_lo;
-            int page = pidx < C::MAXP ? pages[pidx] : __ldg(bt + key0 / bs);
-            if (page < 0 || page >= p.num_blocks) {
-              set_dev_error(p.err, PKV_EDEV_RANGE);
-              page = p.num_blocks;  // out-of-range box: TMA fills zeros
-            }
-            const uint32_t dst0 =
-                sbase + C::RING_OFF + slot * C::SLOT_BYTES + rb * box_rows * 128;
-#pragma unroll
-            for (int cb = 0; cb < C::NBOX; ++cb) {
-              const int col = lo + cb * C::BOX_COLS;
-              if (p.layout == PKV_NHD)
-                tc5::tma_load_4d(dst0 + cb * 2048, &kv_map, col, un.g, key0 % bs, page,
-                                 slot_full(slot));
-              else
-                tc5::tma_load_4d(dst0 + cb * 2048, &kv_map, col, key0 % bs, un.g, page,
-                                 slot_full(slot));
-            }
+                                     static_cast<uint32_t>(HPC * per_head * box_rows * 128));
+        __syncwarp();
+        const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
+        const int nboxes = head_boxes ? C::NBOX : HPC * per_head;
+        for (int i = lane; i < nboxes; i += 32) {
+          const int h = head_boxes ? 0 : i / per_head;
+          const int rem = head_boxes ? i : i - h * per_head;
+          const int rb = rem / C::NBOX, cb = rem - rb * C::NBOX;
+          const int key0 = kb + rb * box_rows;
+          const int pidx = key0 / bs - un.page_lo;
+          int page = pidx < C::MAXP ? pages[pidx] : __ldg(bt + key0 / bs);
+          if (page < 0 || page >= p.num_blocks) {
+            set_dev_error(p.err, PKV_EDEV_RANGE);
+            page = p.num_blocks;  // out-of-range box: TMA fills zeros
           }
+          const uint32_t dst = st + cb * C::CB_STRIDE + h * C::CB_BYTES + rb * box_rows * 128;
+          const int col = lo + cb * C::BOX_COLS;
+          const int head = un.hb * HPC + h;
+          if (head_boxes)  // (col, slot, head, page) in both layouts
+            tc5::tma_load_4d(dst, &kv_map, col, key0 % bs, head, page, slot_full(slot));
+          else if (p.layout == PKV_NHD)
+            tc5::tma_load_4d(dst, &kv_map, col, head, key0 % bs, page, slot_full(slot));
+          else
+            tc5::tma_load_4d(dst, &kv_map, col, key0 % bs, head, page, slot_full(slot));
         }
-        gc += nbatch;
+        ++gc;
+        if (k == k_stage && alive) stage_next();
       }
       ++qi_n;
-      if (alive) stage_next();
     }
     if (alive) {  // end marker for the consumers
       const uint32_t qslot = qs_n % C::NQ;
@@ -393,14 +481,227 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc5::mbar_wait(slot_full(k % NSLOT), (k / NSLOT) & 1u, abort_flag, p.err, false);
     cp_async_wait<0>();
     __syncwarp();
+  } else if constexpr (C::NARROW) {
+    // --------------------------------------- consumer warps, narrow form --
+    // A head's rows fit in 8 (q_len * G <= 8): S^T = K Q^T with the 16 keys
+    // of a step as M and the rows as N = 8, then O^T += V^T P^T with V's
+    // columns as M.  Half the MMAs of the row-major form, whose 16-row tiles
+    // would be at least half padding; P^T reaches the B operand through two
+    // in-register 8x8 transposes.
+    const int cw = warp - 1;
+    const int grp = cw / WG, wig = cw % WG;
+    const int hg = grp;  // one chunk class: group = head of the block
+    const int gr = lane >> 2, qd = lane & 3;
+    uint32_t gc = 0, qc = 0;
+    uint32_t xk = 0;  // 16-key steps processed: picks the exchange buffer
+    float* sbuf = reinterpret_cast<float*>(smem + C::SBUF_OFF) + grp * 2 * WG * 32 * 4;
+    auto group_sync = [&]() {
+      if constexpr (WG == 1)
+        __syncwarp();
+      else
+        named_barrier(2 + grp, 32 * WG);
+    };
+    auto wait_all = [&](uint32_t b, uint32_t parity) {
+      const bool r = tc5::mbar_wait(b, parity, abort_flag, p.err);
+      return __all_sync(0xffffffffu, r);
+    };
+    constexpr int MT = C::DVS / 16;  // 16-column V tiles of this warp
+    for (;;) {
+      const uint32_t qslot = qc % C::NQ;
+      wait_all(q_full(qslot), (qc / C::NQ) & 1u);
+      // the warps of a group take the same decision to stop after a timeout
+      if constexpr (WG > 1) {
+        if (barrier_or(2 + grp, 32 * WG, *abort_flag != 0)) break;
+      } else {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      }
+      const Unit un = *desc_of(qslot);
+      if (un.nch < 0) break;
+      const int kvh = un.hb * HPC + hg;
+      const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES + hg * C::QH_BYTES;
+      // Q^T fragments (B operand) of rows 0..7 over this warp's k-steps
+      uint32_t qb[C::KSW][2];
+#pragma unroll
+      for (int kk = 0; kk < C::KSW; kk += 2) {
+        const int ks = wig * C::KSW + kk;
+        uint32_t r[4];
+        ldmatrix_x4(r, q_piece<C::DK>(qsrc, lane & 7, 2 * ks + (lane >> 3)));
+        qb[kk][0] = r[0];
+        qb[kk][1] = r[1];
+        qb[kk + 1][0] = r[2];
+        qb[kk + 1][1] = r[3];
+      }
+      __syncwarp();
+      if (lane == 0) tc5::mbar_arrive(q_empty(qslot));
+      ++qc;
+
+      // rows 2qd and 2qd + 1 of this thread: visibility
+      int vis_end[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = 2 * qd + j;
+        if (r < un.nrows) {
+          const int i = (un.row0 + r) / G;
+          vis_end[j] = min(un.khi, max(0, min(un.L, un.L - un.qlen + i + 1)));
+        } else {
+          vis_end[j] = 0;
+        }
+      }
+      const float qk_scale = p.softmax_scale * kLog2e;
+      const int kc0 = (p.k_off - lo) * C::ESZ / 16;
+      const int vc0 = (p.v_off - lo) * C::ESZ / 16;
+      const int vcol0 = wig * C::DVS;
+
+      float o[MT][4];  // O^T: V columns (gr, gr + 8 of each tile) x rows (2qd, 2qd + 1)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      float m_run[2] = {-INFINITY, -INFINITY};
+      float l_run[2] = {0.f, 0.f};
+
+      for (int k = 0; k < un.nch; ++k) {
+        const uint32_t c = gc + k;
+        const uint32_t slot = c % NSLOT;
+        const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES + hg * C::CB_BYTES;
+        wait_all(slot_full(slot), (c / NSLOT) & 1u);
+        const int kb = un.klo + k * KPC;
+        if (kb + KPC > un.kmax) {
+          // rows past the last visible key: zero them before anyone reads
+          const int r0 = un.kmax - kb;
+          const int n = (KPC - r0) * C::NBOX * 8;
+          for (int i = wig * 32 + lane; i < n; i += 32 * WG) {
+            const int row = r0 + i / (C::NBOX * 8);
+            const int piece = i % (C::NBOX * 8);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                             slot_piece<C::CB_STRIDE>(st, row, piece)),
+                         "r"(0u)
+                         : "memory");
+          }
+          tc5::fence_proxy_async_smem();
+          group_sync();
+        }
+        const int nsteps = min(KPC / 16, (un.kmax - kb + 15) / 16);
+        for (int ks16 = 0; ks16 < nsteps; ++ks16) {
+          const int r16 = 16 * ks16;
+          const int kb16 = kb + r16;
+          // ---- S^T = K Q^T over this warp's K slice ----
+          float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+          const int mj = lane >> 3;  // the 8x8 matrix this lane addresses
+#pragma unroll
+          for (int kk = 0; kk < C::KSW; ++kk) {
+            const int ks = wig * C::KSW + kk;
+            uint32_t kf[4];
+            ldmatrix_x4(kf, slot_piece<C::CB_STRIDE>(st, r16 + (lane & 7) + 8 * (mj & 1),
+                                                    kc0 + 2 * ks + (mj >> 1)));
+            if (kk & 1)
+              mma_16816<false>(s2, kf, qb[kk][0], qb[kk][1]);
+            else
+              mma_16816<false>(s, kf, qb[kk][0], qb[kk][1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[e] += s2[e];
+          if constexpr (WG > 1) {  // sum the K-slice partial scores of the group
+            const int buf = xk & 1u;
+            *reinterpret_cast<float4*>(sbuf + ((buf * WG + wig) * 32 + lane) * 4) =
+                make_float4(s[0], s[1], s[2], s[3]);
+            group_sync();
+            s[0] = s[1] = s[2] = s[3] = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < WG; ++w2) {
+              const float4 x =
+                  *reinterpret_cast<const float4*>(sbuf + ((buf * WG + w2) * 32 + lane) * 4);
+              s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
+            }
+          }
+          ++xk;
+
+          // ---- online softmax over the keys (M) of rows 2qd + j ----
+          // element e: key kb16 + gr + 8 * (e >> 1), row 2qd + (e & 1)
+          float cmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = kb16 + gr + 8 * (e >> 1);
+            const int j = e & 1;
+            const float v = key < vis_end[j] ? s[e] * qk_scale : -INFINITY;
+            s[e] = v;
+            cmax[j] = fmaxf(cmax[j], v);
+          }
+          float alpha[2], base[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 4));
+            cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 8));
+            cmax[j] = fmaxf(cmax[j], __shfl_xor_sync(0xffffffffu, cmax[j], 16));
+            const float mn = fmaxf(m_run[j], cmax[j]);
+            base[j] = mn == -INFINITY ? 0.f : mn;
+            alpha[j] = fast_exp2(m_run[j] - base[j]);
+            m_run[j] = mn;
+          }
+          float pr[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(s[e] - base[e & 1]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) l_run[j] = l_run[j] * alpha[j] + (pr[j] + pr[j + 2]);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= alpha[0]; o[mt][1] *= alpha[1];
+            o[mt][2] *= alpha[0]; o[mt][3] *= alpha[1];
+          }
+          // P^T as the B operand: keys 0-7 and 8-15, each an 8x8 transpose
+          const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));
+          const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));
+
+          // ---- O^T += V^T P^T over this warp's V columns ----
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, slot_piece<C::CB_STRIDE>(
+                                     st, r16 + (lane & 7) + 8 * (mj >> 1),
+                                     vc0 + (vcol0 + 16 * mt) / 8 + (mj & 1)));
+            mma_16816<false>(o[mt], a, pb0, pb1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc5::mbar_arrive(slot_empty(slot));
+      }
+      gc += un.nch;
+      // row sums: over the 8 lanes that share qd
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = 2 * qd + j;
+        if (r >= un.nrows) continue;
+        const int rr = un.row0 + r;
+        const int64_t t = un.qs + rr / G;
+        const int qh = kvh * G + rr % G;
+        const int64_t orow = (un.s * T + t) * p.num_q_heads + qh;
+        if (l_run[j] > 0.f) {
+          const float inv = 1.f / l_run[j];
+          float* dst = p.partial_o + orow * C::DV + vcol0;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            dst[16 * mt + gr] = o[mt][j] * inv;
+            dst[16 * mt + gr + 8] = o[mt][2 + j] * inv;
+          }
+        }
+        if (wig == 0 && gr == 0)
+          p.partial_lse[orow] =
+              l_run[j] > 0.f ? (m_run[j] + fast_log2(l_run[j])) * kLn2 : -INFINITY;
+      }
+    }
   } else {
     // ------------------------------------------------ consumer warps ----
     const int cw = warp - 1;
     const int grp = cw / WG, wig = cw % WG;
+    const int hg = grp % HPC;  // head of the block this group handles
+    const int ng = grp / HPC;  // chunk class: chunks c with c % NG == ng
     const int gr = lane >> 2, qd = lane & 3;
-    const int ctid = threadIdx.x - 32;  // consumer thread index
     uint32_t gc = 0, qc = 0;
-    uint32_t xk = 0;  // chunks this group has processed: picks the exchange buffer
+    uint32_t xk = 0;  // 16-key steps this group has processed: picks the exchange buffer
     float* sbuf = reinterpret_cast<float*>(smem + C::SBUF_OFF) + grp * 2 * WG * 32 * 8;
     auto group_sync = [&]() {
       if constexpr (WG == 1)
@@ -416,11 +717,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // ---- next staged unit: descriptor and Q fragments ----
       const uint32_t qslot = qc % C::NQ;
       wait_all(q_full(qslot), (qc / C::NQ) & 1u);
-      // every consumer warp takes the same decision to stop after a timeout
-      if (barrier_or(15, 32 * C::NCW, *abort_flag != 0)) break;
+      // The warps that meet at named barriers take the same decision to stop
+      // after a timeout: all consumer warps when the classes merge, else the
+      // warps of one group.
+      if constexpr (NG > 1) {
+        if (barrier_or(15, 32 * C::NCW, *abort_flag != 0)) break;
+      } else if constexpr (WG > 1) {
+        if (barrier_or(2 + grp, 32 * WG, *abort_flag != 0)) break;
+      } else {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      }
       const Unit un = *desc_of(qslot);
       if (un.nch < 0) break;
-      const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES;
+      const int kvh = un.hb * HPC + hg;  // this group's KV head
+      const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES + hg * C::QH_BYTES;
       uint32_t qa[FP8 ? C::UPW : C::KSW][FP8 ? 16 : 4];
       if constexpr (!FP8) {
 #pragma unroll
@@ -469,7 +779,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       float qk_scale = p.softmax_scale * kLog2e;
       float v_mul = 1.f;
       if constexpr (FP8) {
-        const int sidx = p.scale_mode == PKV_SCALE_HEAD ? un.g : 0;
+        const int sidx = p.scale_mode == PKV_SCALE_HEAD ? kvh : 0;
         qk_scale *= __ldg(p.k_scale + sidx);
         v_mul = __ldg(p.v_scale + sidx);
       }
@@ -483,185 +793,193 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       float m_run[2] = {-INFINITY, -INFINITY};
       float l_run[2] = {0.f, 0.f};
 
-      // Chunk c (counted over all units) belongs to group c % NG, and
-      // NSLOT % NG == 0, so a ring slot is only ever consumed by one group,
+      // Chunk c (counted over all units) belongs to class c % NG, and
+      // NSLOT % NG == 0, so a ring slot is only ever consumed by one class,
       // in order: when a group waits for chunk c, the slot's previous chunk
-      // c - NSLOT was its own and has completed, and the parity wait cannot
-      // be satisfied by the phase of chunk c - 2 * NSLOT.
-      const int k_first = static_cast<int>((grp + NG - static_cast<int>(gc % NG)) % NG);
+      // c - NSLOT was its class's own and has completed, and the parity wait
+      // cannot be satisfied by the phase of chunk c - 2 * NSLOT.
+      const int k_first = static_cast<int>((ng + NG - static_cast<int>(gc % NG)) % NG);
       for (int k = k_first; k < un.nch; k += NG) {
         const uint32_t c = gc + k;
         const uint32_t slot = c % NSLOT;
-        const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
+        const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES + hg * C::CB_BYTES;
         wait_all(slot_full(slot), (c / NSLOT) & 1u);
-        const int kb = un.klo + k * 16;
-        if (kb + 16 > un.kmax) {
+        const int kb = un.klo + k * KPC;
+        if (kb + KPC > un.kmax) {
           // rows past the last visible key: zero them before anyone reads
           const int r0 = un.kmax - kb;
-          const int n = (16 - r0) * C::NBOX * 8;
+          const int n = (KPC - r0) * C::NBOX * 8;
           for (int i = wig * 32 + lane; i < n; i += 32 * WG) {
             const int row = r0 + i / (C::NBOX * 8);
             const int piece = i % (C::NBOX * 8);
             asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};\n" ::"r"(
-                             slot_piece(st, row, piece)),
+                             slot_piece<C::CB_STRIDE>(st, row, piece)),
                          "r"(0u)
                          : "memory");
           }
           tc5::fence_proxy_async_smem();
           group_sync();
         }
+        const int nsteps = min(KPC / 16, (un.kmax - kb + 15) / 16);
+        for (int ks16 = 0; ks16 < nsteps; ++ks16) {
+          const int r16 = 16 * ks16;  // first row of this 16-key step in the slot
+          const int kb16 = kb + r16;
 
-        // ---- S = Q K^T over this warp's K slice (two n8 tiles of keys) ----
-        float s[2][4];
+          // ---- S = Q K^T over this warp's K slice (two n8 tiles of keys) ----
+          float s[2][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
-        if constexpr (!FP8) {
-          float s2[2][4];
+          for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+          if constexpr (!FP8) {
+            float s2[2][4];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
+            for (int t = 0; t < 2; ++t) s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
 #pragma unroll
-          for (int kk = 0; kk < C::KSW; ++kk) {
-            const int ks = wig * C::KSW + kk;
-            const int m = lane >> 3;
-            const int row = (m >> 1) * 8 + (lane & 7);
-            uint32_t kf[4];
-            ldmatrix_x4(kf, slot_piece(st, row, kc0 + ks * 2 + (m & 1)));
-            // two accumulator chains per tile for more independent MMAs
-            if (kk & 1) {
-              mma_16816<false>(s2[0], qa[kk], kf[0], kf[1]);
-              mma_16816<false>(s2[1], qa[kk], kf[2], kf[3]);
-            } else {
-              mma_16816<false>(s[0], qa[kk], kf[0], kf[1]);
-              mma_16816<false>(s[1], qa[kk], kf[2], kf[3]);
+            for (int kk = 0; kk < C::KSW; ++kk) {
+              const int ks = wig * C::KSW + kk;
+              const int m = lane >> 3;
+              const int row = r16 + (m >> 1) * 8 + (lane & 7);
+              uint32_t kf[4];
+              ldmatrix_x4(kf, slot_piece<C::CB_STRIDE>(st, row, kc0 + ks * 2 + (m & 1)));
+              // two accumulator chains per tile for more independent MMAs
+              if (kk & 1) {
+                mma_16816<false>(s2[0], qa[kk], kf[0], kf[1]);
+                mma_16816<false>(s2[1], qa[kk], kf[2], kf[3]);
+              } else {
+                mma_16816<false>(s[0], qa[kk], kf[0], kf[1]);
+                mma_16816<false>(s[1], qa[kk], kf[2], kf[3]);
+              }
             }
-          }
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
+            for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[t][e] += s2[t][e];
-        } else {
+              for (int e = 0; e < 4; ++e) s[t][e] += s2[t][e];
+          } else {
 #pragma unroll
-          for (int uu = 0; uu < C::UPW; ++uu) {
-            const int un_ = wig + uu * WG;
-            if (un_ < C::NU) {
+            for (int uu = 0; uu < C::UPW; ++uu) {
+              const int un_ = wig + uu * WG;
+              if (un_ < C::NU) {
 #pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const uint4 kw = lds128(slot_piece(st, 8 * t + gr, kc0 + 4 * un_ + qd));
-                const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
+                for (int t = 0; t < 2; ++t) {
+                  const uint4 kw =
+                      lds128(slot_piece<C::CB_STRIDE>(st, r16 + 8 * t + gr, kc0 + 4 * un_ + qd));
+                  const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint32_t a[4] = {qa[uu][2 * j], qa[uu][8 + 2 * j],
-                                         qa[uu][2 * j + 1], qa[uu][8 + 2 * j + 1]};
-                  mma_16816<true>(s[t], a, e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j])),
-                                  e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j] >> 16)));
+                  for (int j = 0; j < 4; ++j) {
+                    const uint32_t a[4] = {qa[uu][2 * j], qa[uu][8 + 2 * j],
+                                           qa[uu][2 * j + 1], qa[uu][8 + 2 * j + 1]};
+                    mma_16816<true>(s[t], a, e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j])),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j] >> 16)));
+                  }
                 }
               }
             }
           }
-        }
-        if constexpr (WG > 1) {  // sum the K-slice partial scores of the group
-          const int buf = xk & 1u;
-          float* mine = sbuf + (buf * WG + wig) * 32 * 8 + lane * 8;
-          *reinterpret_cast<float4*>(mine) = make_float4(s[0][0], s[0][1], s[0][2], s[0][3]);
-          *reinterpret_cast<float4*>(mine + 4) = make_float4(s[1][0], s[1][1], s[1][2], s[1][3]);
-          group_sync();
+          if constexpr (WG > 1) {  // sum the K-slice partial scores of the group
+            const int buf = xk & 1u;
+            float* mine = sbuf + (buf * WG + wig) * 32 * 8 + lane * 8;
+            *reinterpret_cast<float4*>(mine) = make_float4(s[0][0], s[0][1], s[0][2], s[0][3]);
+            *reinterpret_cast<float4*>(mine + 4) = make_float4(s[1][0], s[1][1], s[1][2], s[1][3]);
+            group_sync();
 #pragma unroll
-          for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+            for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
-          for (int w2 = 0; w2 < WG; ++w2) {
-            const float* src = sbuf + (buf * WG + w2) * 32 * 8 + lane * 8;
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            const float4 y = *reinterpret_cast<const float4*>(src + 4);
-            s[0][0] += x.x; s[0][1] += x.y; s[0][2] += x.z; s[0][3] += x.w;
-            s[1][0] += y.x; s[1][1] += y.y; s[1][2] += y.z; s[1][3] += y.w;
+            for (int w2 = 0; w2 < WG; ++w2) {
+              const float* src = sbuf + (buf * WG + w2) * 32 * 8 + lane * 8;
+              const float4 x = *reinterpret_cast<const float4*>(src);
+              const float4 y = *reinterpret_cast<const float4*>(src + 4);
+              s[0][0] += x.x; s[0][1] += x.y; s[0][2] += x.z; s[0][3] += x.w;
+              s[1][0] += y.x; s[1][1] += y.y; s[1][2] += y.z; s[1][3] += y.w;
+            }
           }
-        }
+          ++xk;
 
-        // ---- online softmax (rows gr, gr + 8), log2 domain ----
-        float cmax[2] = {-INFINITY, -INFINITY};
+          // ---- online softmax (rows gr, gr + 8), log2 domain ----
+          float cmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int key = kb + 8 * t + 2 * qd + (e & 1);
-            const int kr = e >> 1;
-            const float v = key < vis_end[kr] ? s[t][e] * qk_scale : -INFINITY;
-            s[t][e] = v;
-            cmax[kr] = fmaxf(cmax[kr], v);
+            for (int e = 0; e < 4; ++e) {
+              const int key = kb16 + 8 * t + 2 * qd + (e & 1);
+              const int kr = e >> 1;
+              const float v = key < vis_end[kr] ? s[t][e] * qk_scale : -INFINITY;
+              s[t][e] = v;
+              cmax[kr] = fmaxf(cmax[kr], v);
+            }
+          float alpha[2], base[2];
+#pragma unroll
+          for (int kr = 0; kr < 2; ++kr) {
+            cmax[kr] = fmaxf(cmax[kr], __shfl_xor_sync(0xffffffffu, cmax[kr], 1));
+            cmax[kr] = fmaxf(cmax[kr], __shfl_xor_sync(0xffffffffu, cmax[kr], 2));
+            const float mn = fmaxf(m_run[kr], cmax[kr]);
+            base[kr] = mn == -INFINITY ? 0.f : mn;
+            alpha[kr] = fast_exp2(m_run[kr] - base[kr]);
+            m_run[kr] = mn;
           }
-        float alpha[2], base[2];
+          float psum[2] = {0.f, 0.f};
 #pragma unroll
-        for (int kr = 0; kr < 2; ++kr) {
-          cmax[kr] = fmaxf(cmax[kr], __shfl_xor_sync(0xffffffffu, cmax[kr], 1));
-          cmax[kr] = fmaxf(cmax[kr], __shfl_xor_sync(0xffffffffu, cmax[kr], 2));
-          const float mn = fmaxf(m_run[kr], cmax[kr]);
-          base[kr] = mn == -INFINITY ? 0.f : mn;
-          alpha[kr] = fast_exp2(m_run[kr] - base[kr]);
-          m_run[kr] = mn;
-        }
-        float psum[2] = {0.f, 0.f};
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float pv = fast_exp2(s[t][e] - base[e >> 1]);
-            s[t][e] = pv;
-            psum[e >> 1] += pv;
-          }
-#pragma unroll
-        for (int kr = 0; kr < 2; ++kr) l_run[kr] = l_run[kr] * alpha[kr] + psum[kr];
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
-          o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
-          o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
-        }
-        uint32_t pa[4];
-        if constexpr (!FP8) {
-          pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-          pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-          pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-          pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-        } else {
-          pa[0] = pack_f16x2(s[0][0], s[0][1]);
-          pa[1] = pack_f16x2(s[0][2], s[0][3]);
-          pa[2] = pack_f16x2(s[1][0], s[1][1]);
-          pa[3] = pack_f16x2(s[1][2], s[1][3]);
-        }
-
-        // ---- O += P V over this warp's V columns ----
-        if constexpr (!FP8) {
-#pragma unroll
-          for (int np = 0; np < C::NT / 2; ++np) {
-            const int m = lane >> 3;
-            const int row = (m & 1) * 8 + (lane & 7);
-            uint32_t r[4];
-            ldmatrix_x4_trans(r, slot_piece(st, row, vc0 + (vcol0 + 16 * np) / 8 + (m >> 1)));
-            mma_16816<false>(o[2 * np], pa, r[0], r[1]);
-            mma_16816<false>(o[2 * np + 1], pa, r[2], r[3]);
-          }
-        } else {
-#pragma unroll
-          for (int vb = 0; vb < C::DVS / 128; ++vb) {
-            const int piece = vc0 + (vcol0 + 128 * vb) / 16 + gr;
-            const int rows[4] = {2 * qd, 2 * qd + 1, 2 * qd + 8, 2 * qd + 9};
-            uint32_t kw[4][4];
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const uint4 v = lds128(slot_piece(st, rows[k4], piece));
-              kw[k4][0] = v.x; kw[k4][1] = v.y; kw[k4][2] = v.z; kw[k4][3] = v.w;
+            for (int e = 0; e < 4; ++e) {
+              const float pv = fast_exp2(s[t][e] - base[e >> 1]);
+              s[t][e] = pv;
+              psum[e >> 1] += pv;
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int wd = j >> 2, sel = j & 3;
-              const uint32_t b0 = e4m3x2_to_f16x2(pick_bytes(kw[0][wd], kw[1][wd], sel));
-              const uint32_t b1 = e4m3x2_to_f16x2(pick_bytes(kw[2][wd], kw[3][wd], sel));
-              mma_16816<true>(o[16 * vb + j], pa, b0, b1);
+          for (int kr = 0; kr < 2; ++kr) l_run[kr] = l_run[kr] * alpha[kr] + psum[kr];
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) {
+            o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+          }
+          uint32_t pa[4];
+          if constexpr (!FP8) {
+            pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+            pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+            pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+            pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+          } else {
+            pa[0] = pack_f16x2(s[0][0], s[0][1]);
+            pa[1] = pack_f16x2(s[0][2], s[0][3]);
+            pa[2] = pack_f16x2(s[1][0], s[1][1]);
+            pa[3] = pack_f16x2(s[1][2], s[1][3]);
+          }
+
+          // ---- O += P V over this warp's V columns ----
+          if constexpr (!FP8) {
+#pragma unroll
+            for (int np = 0; np < C::NT / 2; ++np) {
+              const int m = lane >> 3;
+              const int row = r16 + (m & 1) * 8 + (lane & 7);
+              uint32_t r[4];
+              ldmatrix_x4_trans(
+                  r, slot_piece<C::CB_STRIDE>(st, row, vc0 + (vcol0 + 16 * np) / 8 + (m >> 1)));
+              mma_16816<false>(o[2 * np], pa, r[0], r[1]);
+              mma_16816<false>(o[2 * np + 1], pa, r[2], r[3]);
+            }
+          } else {
+#pragma unroll
+            for (int vb = 0; vb < C::DVS / 128; ++vb) {
+              const int piece = vc0 + (vcol0 + 128 * vb) / 16 + gr;
+              const int rows[4] = {r16 + 2 * qd, r16 + 2 * qd + 1, r16 + 2 * qd + 8,
+                                   r16 + 2 * qd + 9};
+              uint32_t kw[4][4];
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const uint4 v = lds128(slot_piece<C::CB_STRIDE>(st, rows[k4], piece));
+                kw[k4][0] = v.x; kw[k4][1] = v.y; kw[k4][2] = v.z; kw[k4][3] = v.w;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int wd = j >> 2, sel = j & 3;
+                const uint32_t b0 = e4m3x2_to_f16x2(pick_bytes(kw[0][wd], kw[1][wd], sel));
+                const uint32_t b1 = e4m3x2_to_f16x2(pick_bytes(kw[2][wd], kw[3][wd], sel));
+                mma_16816<true>(o[16 * vb + j], pa, b0, b1);
+              }
             }
           }
         }
         __syncwarp();
         if (lane == 0) tc5::mbar_arrive(slot_empty(slot));
-        ++xk;
       }
       gc += un.nch;
 #pragma unroll
@@ -676,16 +994,66 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           return vcol0 + 128 * (nt / 16) + 16 * (2 * qd + e) + (nt % 16);
       };
 
-      if constexpr (NG == 1) {
-        // one group: every warp writes its own V columns of the partial
+      if constexpr (NG > 1) {
+        // ---- every chunk class hands its (O, max, sum) of each row over;
+        //      then all consumer threads combine the classes element-wise ----
+        float* mo = reinterpret_cast<float*>(smem + C::MERGE_OFF);
+        auto mrow = [&](int q, int h, int r) { return mo + ((q * HPC + h) * 16 + r) * C::MROW; };
+        named_barrier(1, 32 * C::NCW);  // the previous unit's reads are done
+#pragma unroll
+        for (int kr = 0; kr < 2; ++kr) {
+          float* b = mrow(ng, hg, gr + 8 * kr);
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) b[col_of(nt, e)] = o[nt][2 * kr + e];
+          if (wig == 0 && qd == 0) {
+            b[C::DVP] = m_run[kr];
+            b[C::DVP + 1] = l_run[kr];
+          }
+        }
+        named_barrier(1, 32 * C::NCW);
+        const int ctid = threadIdx.x - 32;
+        const int per_head = un.nrows * C::DV;
+        for (int idx = ctid; idx < HPC * per_head; idx += 32 * C::NCW) {
+          const int h = idx / per_head;
+          const int rc = idx - h * per_head;
+          const int r = rc / C::DV, cc = rc - r * C::DV;
+          float M = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < NG; ++q) M = fmaxf(M, mrow(q, h, r)[C::DVP]);
+          const int rr = un.row0 + r;
+          const int64_t t = un.qs + rr / G;
+          const int kvh2 = un.hb * HPC + h;
+          const int64_t orow = (un.s * T + t) * p.num_q_heads + kvh2 * G + rr % G;
+          if (M == -INFINITY) {  // no class saw a key of this row
+            if (cc == 0) p.partial_lse[orow] = -INFINITY;
+            continue;
+          }
+          float l = 0.f, acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < NG; ++q) {
+            const float* b = mrow(q, h, r);
+            const float wq = fast_exp2(b[C::DVP] - M);  // 0 for a class without keys
+            l += wq * b[C::DVP + 1];
+            acc += wq * b[cc];
+          }
+          float vm = 1.f;
+          if constexpr (FP8)
+            vm = __ldg(p.v_scale + (p.scale_mode == PKV_SCALE_HEAD ? kvh2 : 0));
+          p.partial_o[orow * C::DV + cc] = acc / l * vm;
+          if (cc == 0) p.partial_lse[orow] = (M + fast_log2(l)) * kLn2;
+        }
+      } else {
+        // every warp writes its own V columns of the head's partial rows
 #pragma unroll
         for (int kr = 0; kr < 2; ++kr) {
           const int r = gr + 8 * kr;
           if (r >= un.nrows) continue;
           const int rr = un.row0 + r;
           const int64_t t = un.qs + rr / G;
-          const int h = un.g * G + rr % G;
-          const int64_t orow = (un.s * T + t) * p.num_q_heads + h;
+          const int qh = kvh * G + rr % G;
+          const int64_t orow = (un.s * T + t) * p.num_q_heads + qh;
           if (l_run[kr] > 0.f) {
             const float inv = v_mul / l_run[kr];
             float* dst = p.partial_o + orow * C::DV;
@@ -698,52 +1066,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             p.partial_lse[orow] =
                 l_run[kr] > 0.f ? (m_run[kr] + fast_log2(l_run[kr])) * kLn2 : -INFINITY;
         }
-      } else {
-        // ---- merge the groups through shared memory ----
-        float* so = reinterpret_cast<float*>(smem + C::MERGE_OFF);  // [NG][16][DVP]
-        float* sm = so + NG * 16 * C::DVP;                          // [NG][16]
-        float* sl = sm + NG * 16;                                   // [NG][16]
-        named_barrier(1, 32 * C::NCW);  // previous unit's merge reads done
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            so[(grp * 16 + gr) * C::DVP + col_of(nt, e)] = o[nt][e];
-            so[(grp * 16 + gr + 8) * C::DVP + col_of(nt, e)] = o[nt][2 + e];
-          }
-        if (wig == 0 && qd == 0) {
-          sm[grp * 16 + gr] = m_run[0];
-          sm[grp * 16 + gr + 8] = m_run[1];
-          sl[grp * 16 + gr] = l_run[0];
-          sl[grp * 16 + gr + 8] = l_run[1];
-        }
-        named_barrier(1, 32 * C::NCW);
-        for (int idx = ctid; idx < un.nrows * C::DV; idx += 32 * C::NCW) {
-          const int r = idx / C::DV;
-          const int cc = idx - r * C::DV;
-          const int rr = un.row0 + r;
-          const int64_t t = un.qs + rr / G;
-          const int h = un.g * G + rr % G;
-          float M = -INFINITY;
-#pragma unroll
-          for (int q = 0; q < NG; ++q) M = fmaxf(M, sm[q * 16 + r]);
-          const int64_t orow = (un.s * T + t) * p.num_q_heads + h;
-          if (M == -INFINITY) {
-            if (cc == 0) p.partial_lse[orow] = -INFINITY;
-            continue;
-          }
-          float lsum = 0.f, acc = 0.f;
-#pragma unroll
-          for (int q = 0; q < NG; ++q) {
-            const float mq = sm[q * 16 + r];
-            if (mq == -INFINITY) continue;
-            const float wq = fast_exp2(mq - M);
-            lsum += wq * sl[q * 16 + r];
-            acc += wq * so[(q * 16 + r) * C::DVP + cc];
-          }
-          p.partial_o[orow * C::DV + cc] = acc / lsum * v_mul;
-          if (cc == 0) p.partial_lse[orow] = (M + fast_log2(lsum)) * kLn2;
-        }
       }
     }
   }
@@ -755,23 +1077,40 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(decode_kernel<C>, C::SMEM, attr_set);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap kv_map;
-  const int box_rows = p.block_size < 16 ? p.block_size : 16;
-  if (!make_cache_tmap(&kv_map, p.cache, p.dtype, p.layout, p.num_blocks,
-                       p.block_size, p.num_kv_heads, p.row_elems, C::BOX_COLS,
-                       box_rows))
-    return cudaErrorInvalidValue;
+  const int box_rows = box_rows_for(p.block_size, C::KPC);
+  // one box for all HPC heads of a column slice when a chunk's keys are one
+  // box high (5 boxes per 16-key chunk of 4 heads instead of 20)
+  const int head_boxes = C::HPC > 1 && box_rows == C::KPC ? 1 : 0;
+  const bool ok =
+      head_boxes ? make_cache_tmap_heads(&kv_map, p.cache, p.dtype, p.layout, p.num_blocks,
+                                         p.block_size, p.num_kv_heads, p.row_elems,
+                                         C::BOX_COLS, box_rows, C::HPC)
+                 : make_cache_tmap(&kv_map, p.cache, p.dtype, p.layout, p.num_blocks,
+                                   p.block_size, p.num_kv_heads, p.row_elems, C::BOX_COLS,
+                                   box_rows);
+  if (!ok) return cudaErrorInvalidValue;
   const int64_t RG = (static_cast<int64_t>(p.max_query_len) * p.group + 15) / 16;
-  const int64_t units = static_cast<int64_t>(p.num_splits) * p.num_seqs * p.num_kv_heads * RG;
+  const int64_t units = static_cast<int64_t>(p.num_splits) * p.num_seqs *
+                        (p.num_kv_heads / C::HPC) * RG;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, p);
+  decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, p, head_boxes);
   return cudaGetLastError();
 }
 
-// <DK, DV, fp8, warps per group, groups, ring slots, unit slots, staged span>
-using CfgBf16_192 = DecodeCfg<192, 128, false, 1, 6, 12, 4, 320>;
-using CfgFp8_192 = DecodeCfg<192, 128, true, 1, 6, 18, 4, 320>;
-using CfgBf16_576 = DecodeCfg<576, 512, false, 4, 1, 7, 3, 576>;
-using CfgFp8_576 = DecodeCfg<576, 512, true, 4, 1, 12, 3, 576>;
+// <DK, DV, fp8, heads per chunk, warps per group, chunk classes, keys per
+//  chunk, ring slots, unit slots, staged span>
+// K192 / V128, bf16: four heads per chunk (40 KB of 16 keys) when Hkv
+// allows, else one head with six chunk classes.
+using CfgBf16_192x4 = DecodeCfg<192, 128, false, 4, 2, 1, 16, 4, 2, 320>;
+// the same with a head's rows in 8 (q_len * G <= 8): transposed MMAs
+using CfgBf16_192x4n = DecodeCfg<192, 128, false, 4, 2, 1, 16, 4, 2, 320, true>;
+using CfgBf16_192x1 = DecodeCfg<192, 128, false, 1, 1, 6, 16, 12, 4, 320>;
+// K192 / V128, fp8: one head, 64 keys per chunk (three 8 KB boxes at block
+// 64), six chunk classes.
+using CfgFp8_192 = DecodeCfg<192, 128, true, 1, 1, 6, 64, 6, 2, 320>;
+// MLA 576 / 512: one latent head, 32 (bf16) or 64 (fp8) keys per chunk.
+using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 4, 2, 576>;
+using CfgFp8_576 = DecodeCfg<576, 512, true, 1, 4, 1, 64, 4, 2, 576>;
 
 }  // namespace
 
@@ -783,9 +1122,12 @@ bool decode_supported(int head_size, int head_size_v, int dtype) {
 
 cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream) {
   const bool fp8 = p.dtype == PKV_FP8_E4M3;
-  if (p.head_size == 192 && p.head_size_v == 128)
-    return fp8 ? launch_cfg<CfgFp8_192>(p, num_sms, stream)
-               : launch_cfg<CfgBf16_192>(p, num_sms, stream);
+  if (p.head_size == 192 && p.head_size_v == 128) {
+    if (fp8) return launch_cfg<CfgFp8_192>(p, num_sms, stream);
+    if (p.num_kv_heads % 4 != 0) return launch_cfg<CfgBf16_192x1>(p, num_sms, stream);
+    return p.max_query_len * p.group <= 8 ? launch_cfg<CfgBf16_192x4n>(p, num_sms, stream)
+                                          : launch_cfg<CfgBf16_192x4>(p, num_sms, stream);
+  }
   if (p.head_size == 576 && p.head_size_v == 512)
     return fp8 ? launch_cfg<CfgFp8_576>(p, num_sms, stream)
                : launch_cfg<CfgBf16_576>(p, num_sms, stream);

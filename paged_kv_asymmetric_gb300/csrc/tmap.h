@@ -62,6 +62,42 @@ inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 4-D map over the cache whose boxes hold `box_heads` consecutive KV heads
+// x `box_rows` token slots x `box_cols` row elements, landing in shared memory
+// as [head][slot][box_cols] (each head's slots contiguous).  Coordinates are
+// (col, slot, head, page) for both layouts, so for NHD the strides do not
+// increase (slot stride H*R*e > head stride R*e); the encoder accepts that and
+// a layout check on GB300 confirmed every element of such boxes.
+inline bool make_cache_tmap_heads(CUtensorMap* map, const void* cache, int dtype,
+                                  int layout, int num_blocks, int block_size,
+                                  int num_kv_heads, int row_elems, int box_cols,
+                                  int box_rows, int box_heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encode_fn();
+  if (encode == nullptr) return false;
+  const cuuint64_t e = dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const cuuint64_t R = static_cast<cuuint64_t>(row_elems);
+  const cuuint64_t H = static_cast<cuuint64_t>(num_kv_heads);
+  const cuuint64_t B = static_cast<cuuint64_t>(block_size);
+  const cuuint64_t dims[4] = {R, B, H, static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[3];
+  if (layout == PKV_NHD) {  // [blk][bs][H][R]
+    strides[0] = H * R * e; strides[1] = R * e; strides[2] = B * H * R * e;
+  } else {                  // [blk][H][bs][R]
+    strides[0] = R * e; strides[1] = B * R * e; strides[2] = H * B * R * e;
+  }
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols),
+                             static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_heads), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode(map,
+                dtype == PKV_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                4, const_cast<void*>(cache), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Sets the dynamic shared-memory limit of `fn` once per device.
 template <class F>
 inline cudaError_t ensure_smem_attr(F* fn, int bytes, int* done) {
