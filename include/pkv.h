@@ -214,10 +214,11 @@ int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
                        void *out, float *lse_out, pkv_stream_t stream);
 
 /*
- * pkv_decode_suggest_splits -- a split count that gives the decode launch
- * about four work units per SM of the current device (a unit covers four KV
- * heads when num_kv_heads is a multiple of 4, else one), for sequences of up
- * to max_seq_len keys, capped so that every segment keeps at least one page.
+ * pkv_decode_suggest_splits -- a split count for the decode launch on the
+ * current device: about one work unit per SM for a single sequence and three
+ * per SM for a batch (a unit covers four KV heads when num_kv_heads is a
+ * multiple of 4, else one), for sequences of up to max_seq_len keys, capped
+ * so that every segment keeps at least 256 keys and one page.
  * Host-only; returns >= 1, or a negative status.
  */
 int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,

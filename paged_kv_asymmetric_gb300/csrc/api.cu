@@ -320,7 +320,13 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
   const int64_t head_units = num_kv_heads % 4 == 0 ? num_kv_heads / 4 : num_kv_heads;
   const int64_t units = static_cast<int64_t>(num_seqs) * head_units *
                         ((max_query_len * G + 15) / 16);
-  int64_t s = (4 * static_cast<int64_t>(sms) + units - 1) / units;
+  // one unit per SM for a single sequence (its units are all alike); about
+  // three per SM for a batch, whose lengths may differ, so that they balance
+  const int64_t per_sm = num_seqs > 1 ? 3 : 1;
+  int64_t s = (per_sm * sms + units - 1) / units;
+  // and at least 256 keys, and one page, per segment
+  const int64_t by_keys = max_seq_len / 256;
+  if (s > by_keys) s = by_keys;
   const int64_t pages = (static_cast<int64_t>(max_seq_len) + block_size - 1) / block_size;
   if (s > pages) s = pages;
   if (s < 1) s = 1;

@@ -88,7 +88,8 @@ struct DecodeCfg {
   static constexpr int QH_BYTES = QROWS * DK * 2;        // one head's Q rows
   static constexpr int Q_BYTES = HPC * QH_BYTES;
   static constexpr int KSTEPS = DK / 16;
-  static constexpr int KSW = KSTEPS / WG;                  // bf16: k-steps per warp
+  // bf16: k-steps per warp, at most (warp w takes [w*KSTEPS/WG, (w+1)*KSTEPS/WG))
+  static constexpr int KSW = (KSTEPS + WG - 1) / WG;
   static constexpr int NU = DK / 64;                       // fp8: 64-wide units
   static constexpr int UPW = (NU + WG - 1) / WG;
   static constexpr int DVS = DV / WG;                      // V columns per warp
@@ -110,14 +111,15 @@ struct DecodeCfg {
   static constexpr int BAR_OFF = SBUF_OFF + SBUF;
   static constexpr int NBAR = 2 * NSLOT + 2 * NQ;
   static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
-  static_assert(DK % 64 == 0 && KSTEPS % WG == 0, "K slices");
+  static_assert(DK % 64 == 0, "K in 64-column units");
   static_assert(DV % WG == 0 && DVS % (FP8 ? 128 : 16) == 0, "V slices");
   static_assert(QCH % 8 == 0, "Q rows in whole 128-byte groups");
   static_assert(KPC % 16 == 0 && KPC <= 256, "keys per chunk");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(NSLOT % NG == 0, "each ring slot belongs to one chunk class");
   static_assert(NGRP + 2 <= 15, "named barrier ids");
-  static_assert(!NARROW || (!FP8 && NG == 1 && KSW % 2 == 0 && DVS % 16 == 0),
+  static_assert(!NARROW || (!FP8 && NG == 1 && KSTEPS % WG == 0 && KSW % 2 == 0 &&
+                             DVS % 16 == 0),
                 "narrow form: bf16, one chunk class, k-step pairs, 16-column V tiles");
 };
 
@@ -731,11 +733,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (un.nch < 0) break;
       const int kvh = un.hb * HPC + hg;  // this group's KV head
       const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES + hg * C::QH_BYTES;
+      // this warp's k-steps of the bf16 path: [ks_lo, ks_lo + nks) (a
+      // compile-time count when WG divides them)
+      constexpr bool kEven = C::KSTEPS % WG == 0;
+      const int ks_lo = kEven ? wig * C::KSW : wig * C::KSTEPS / WG;
+      const int nks = kEven ? C::KSW : (wig + 1) * C::KSTEPS / WG - ks_lo;
       uint32_t qa[FP8 ? C::UPW : C::KSW][FP8 ? 16 : 4];
       if constexpr (!FP8) {
 #pragma unroll
         for (int kk = 0; kk < C::KSW; ++kk) {
-          const int ks = wig * C::KSW + kk;
+          const int ks = ks_lo + (kEven || kk < nks ? kk : 0);
           const int m = lane >> 3;
           const int row = (m & 1) * 8 + (lane & 7);
           ldmatrix_x4(qa[kk], q_piece<C::DK>(qsrc, row, ks * 2 + (m >> 1)));
@@ -835,7 +842,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int t = 0; t < 2; ++t) s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < C::KSW; ++kk) {
-              const int ks = wig * C::KSW + kk;
+              if (!kEven && kk >= nks) break;
+              const int ks = ks_lo + kk;
               const int m = lane >> 3;
               const int row = r16 + (m >> 1) * 8 + (lane & 7);
               uint32_t kf[4];
@@ -854,25 +862,36 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) s[t][e] += s2[t][e];
           } else {
+            // two accumulator chains per tile (j even / odd)
+            float s2[2][4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
 #pragma unroll
             for (int uu = 0; uu < C::UPW; ++uu) {
               const int un_ = wig + uu * WG;
               if (un_ < C::NU) {
+                uint4 kw[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                  kw[t] = lds128(slot_piece<C::CB_STRIDE>(st, r16 + 8 * t + gr, kc0 + 4 * un_ + qd));
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                  const uint4 kw =
-                      lds128(slot_piece<C::CB_STRIDE>(st, r16 + 8 * t + gr, kc0 + 4 * un_ + qd));
-                  const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
+                  const uint32_t wv[4] = {kw[t].x, kw[t].y, kw[t].z, kw[t].w};
 #pragma unroll
                   for (int j = 0; j < 4; ++j) {
                     const uint32_t a[4] = {qa[uu][2 * j], qa[uu][8 + 2 * j],
                                            qa[uu][2 * j + 1], qa[uu][8 + 2 * j + 1]};
-                    mma_16816<true>(s[t], a, e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j])),
+                    mma_16816<true>(j & 1 ? s2[t] : s[t], a,
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j])),
                                     e4m3x2_to_f16x2(static_cast<uint16_t>(wv[j] >> 16)));
                   }
                 }
               }
             }
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) s[t][e] += s2[t][e];
           }
           if constexpr (WG > 1) {  // sum the K-slice partial scores of the group
             const int buf = xk & 1u;

@@ -90,11 +90,13 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One CTA per row for rows with many splits or wide V (dv % 4 == 0): the
-// split maxima and weight sums are block reductions, and the threads form
-// `ngrp` groups over the splits x `cols` lanes over 16-byte column pieces, so
-// that a row with hundreds of splits is read by hundreds of loads in flight
-// instead of one warp's serial walk.
+// One CTA per (row, block of columns) for dv % 4 == 0: the split maxima and
+// weight sums are block reductions (repeated by each column block of a row:
+// S values), and the threads form `ngrp` groups over the splits x `cols`
+// lanes over 16-byte column pieces, so that a row with hundreds of splits is
+// read by hundreds of loads in flight instead of one warp's serial walk.
+// Rows are split into column blocks when there are too few rows to fill the
+// GPU (e.g. one token of an MLA decode with 150+ splits).
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
     splitkv_reduce_rows_kernel(const float* __restrict__ po,
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(THREADS)
   __shared__ float4 part[THREADS];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int r = blockIdx.x;
+  const int ncb = gridDim.y;  // column blocks per row
   auto block_reduce = [&](float v, bool is_max) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -124,9 +127,12 @@ __global__ void __launch_bounds__(THREADS)
     M = fmaxf(M, __ldg(plse + static_cast<int64_t>(s) * rows + r));
   M = block_reduce(M, true);
   __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
+  const int dv4 = dv >> 2;
+  const int cb4 = dv4 / ncb;  // 16-byte pieces of this block
+  const int c4_lo = blockIdx.y * cb4;
   if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
-    for (int c = tid; c < dv; c += THREADS) orow[c] = __float2bfloat16_rn(0.f);
-    if (lse_out != nullptr && tid == 0) lse_out[r] = -INFINITY;
+    for (int c = tid; c < 4 * cb4; c += THREADS) orow[4 * c4_lo + c] = __float2bfloat16_rn(0.f);
+    if (lse_out != nullptr && tid == 0 && blockIdx.y == 0) lse_out[r] = -INFINITY;
     return;
   }
   const float Ml2 = M * kLog2e;
@@ -137,14 +143,14 @@ __global__ void __launch_bounds__(THREADS)
   }
   const float W = block_reduce(wsum, false);
   const float inv = 1.f / W;
-  const int dv4 = dv >> 2;
-  const int cols = dv4 < THREADS ? dv4 : THREADS;
+  const int cols = cb4 < THREADS ? cb4 : THREADS;
   const int ngrp = THREADS / cols;
   const int c = tid % cols, grp = tid / cols;
-  for (int c0 = 0; c0 < dv4; c0 += cols) {
-    const int c4 = c0 + c;
+  for (int c0 = 0; c0 < cb4; c0 += cols) {
+    const int c4 = c4_lo + c0 + c;
+    const bool in = c0 + c < cb4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (grp < ngrp && c4 < dv4) {
+    if (grp < ngrp && in) {
       // four splits per step, their loads independent of each other
       constexpr int U = 4;
       for (int s0 = grp; s0 < S; s0 += U * ngrp) {
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(THREADS)
     __syncthreads();
     part[tid] = acc;
     __syncthreads();
-    if (grp == 0 && c4 < dv4) {
+    if (grp == 0 && in) {
       for (int g2 = 1; g2 < ngrp; ++g2) {
         const float4 v = part[g2 * cols + c];
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
@@ -185,7 +191,7 @@ __global__ void __launch_bounds__(THREADS)
       *reinterpret_cast<uint2*>(orow + 4 * c4) = st;
     }
   }
-  if (lse_out != nullptr && tid == 0) lse_out[r] = M + fast_log2(W) * kLn2;
+  if (lse_out != nullptr && tid == 0 && blockIdx.y == 0) lse_out[r] = M + fast_log2(W) * kLn2;
 }
 
 }  // namespace
@@ -197,7 +203,14 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
                                   cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
   if ((head_size_v & 3) == 0) {
-    splitkv_reduce_rows_kernel<512><<<num_rows, 512, 0, stream>>>(
+    // column blocks (a power of two dividing dv/4, >= 8 pieces each) until
+    // there are about 2 x 152 CTAs
+    const int dv4 = head_size_v >> 2;
+    int ncb = 1;
+    while (static_cast<int64_t>(num_rows) * ncb < 304 && dv4 % (2 * ncb) == 0 &&
+           dv4 / (2 * ncb) >= 8)
+      ncb *= 2;
+    splitkv_reduce_rows_kernel<512><<<dim3(num_rows, ncb), 512, 0, stream>>>(
         partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out);
     return cudaGetLastError();
   }
