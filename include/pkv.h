@@ -215,10 +215,11 @@ int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
 
 /*
  * pkv_decode_suggest_splits -- a split count for the decode launch on the
- * current device: about one work unit per SM for a single sequence and three
- * per SM for a batch (a unit covers four KV heads when num_kv_heads is a
- * multiple of 4, else one), for sequences of up to max_seq_len keys, capped
- * so that every segment keeps at least 256 keys and one page.
+ * current device: one work unit per SM for a single sequence; for a batch
+ * two to four per SM, preferring a unit count that divides evenly over the
+ * SMs (a unit covers four KV heads when num_kv_heads is a multiple of 4, else
+ * one); for sequences of up to max_seq_len keys, capped so that every segment
+ * keeps at least 256 keys and one page.
  * Host-only; returns >= 1, or a negative status.
  */
 int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,

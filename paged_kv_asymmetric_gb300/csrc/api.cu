@@ -320,10 +320,26 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
   const int64_t head_units = num_kv_heads % 4 == 0 ? num_kv_heads / 4 : num_kv_heads;
   const int64_t units = static_cast<int64_t>(num_seqs) * head_units *
                         ((max_query_len * G + 15) / 16);
-  // one unit per SM for a single sequence (its units are all alike); about
-  // three per SM for a batch, whose lengths may differ, so that they balance
-  const int64_t per_sm = num_seqs > 1 ? 3 : 1;
-  int64_t s = (per_sm * sms + units - 1) / units;
+  // One unit per SM for a single sequence (its units are all alike).  For a
+  // batch at least two per SM, and among up to twice that many splits the
+  // count that would leave the fewest SMs idle at the end if the units were
+  // alike (ceil(n / sms) * sms / n), taking more splits only for a gain of
+  // more than 2 %.
+  int64_t s = (sms + units - 1) / units;
+  if (num_seqs > 1) {
+    const int64_t lo = (2 * static_cast<int64_t>(sms) + units - 1) / units;
+    s = lo;
+    int64_t best_num = 1, best_den = 1;  // imbalance of `s` as a fraction
+    for (int64_t c = lo; c <= 2 * lo; ++c) {
+      const int64_t n = c * units;
+      const int64_t num = (n + sms - 1) / sms * sms;  // imbalance = num / n
+      if (c == lo || num * best_den * 100 < best_num * n * 98) {
+        s = c;
+        best_num = num;
+        best_den = n;
+      }
+    }
+  }
   // and at least 256 keys, and one page, per segment
   const int64_t by_keys = max_seq_len / 256;
   if (s > by_keys) s = by_keys;
