@@ -241,6 +241,19 @@ int pkv_supports(int head_size, int head_size_v, int dtype);
  */
 int pkv_get_device_error(int *code, pkv_stream_t stream);
 
+/*
+ * pkv_selftest_bounded_wait -- checks, on the current device, the failure
+ * path that every kernel of the library shares: a one-warp kernel waits on an
+ * mbarrier that nothing arrives on, with the same bounded wait the kernels
+ * use but a limit of `limit_us` microseconds (1 .. 2,000,000); the wait
+ * gives up, records PKV_EDEV_TIMEOUT in the device error word and the kernel
+ * returns, so the context stays usable.  Read the outcome with
+ * pkv_get_device_error.  Not part of the attention path (the pages have no
+ * counterpart); asynchronous on `stream`; PKV_EINVAL for a limit out of
+ * range.
+ */
+int pkv_selftest_bounded_wait(int limit_us, pkv_stream_t stream);
+
 /* The cudaError_t of the last PKV_ECUDA return on the calling thread. */
 int pkv_last_cuda_error(void);
 

@@ -34,7 +34,8 @@ SCALE_NONE, SCALE_TENSOR, SCALE_HEAD = 0, 1, 2
 EXPORTED = (
     "pkv_kv_cache_write", "pkv_paged_attn_prefill", "pkv_paged_attn_decode",
     "pkv_splitkv_reduce", "pkv_decode_suggest_splits", "pkv_supports",
-    "pkv_get_device_error", "pkv_last_cuda_error", "pkv_status_string",
+    "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
+    "pkv_status_string",
 )
 
 
@@ -94,6 +95,7 @@ def _lib():
         lib.pkv_decode_suggest_splits.argtypes = [I, I, I, I, I, I]
         lib.pkv_supports.argtypes = [I, I, I]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
+        lib.pkv_selftest_bounded_wait.argtypes = [I, P]
         lib.pkv_last_cuda_error.argtypes = []
         lib.pkv_status_string.argtypes = [I]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -247,3 +249,10 @@ def get_device_error(stream=None) -> int:
     _check("pkv_get_device_error",
            _lib().pkv_get_device_error(ctypes.byref(code), _stream(stream)))
     return code.value
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> None:
+    """Runs the bounded-wait check (see pkv_selftest_bounded_wait); read
+    the outcome with get_device_error()."""
+    _check("pkv_selftest_bounded_wait",
+           _lib().pkv_selftest_bounded_wait(int(limit_us), _stream(stream)))

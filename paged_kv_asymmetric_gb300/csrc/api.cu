@@ -374,6 +374,16 @@ int pkv_get_device_error(int* code, pkv_stream_t stream) {
   return PKV_OK;
 }
 
+int pkv_selftest_bounded_wait(int limit_us, pkv_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return PKV_EINVAL;
+  int* err = nullptr;
+  int rc = device_info(&err, nullptr);
+  if (rc != PKV_OK) return rc;
+  const cudaError_t e = pkv::launch_bounded_wait_selftest(
+      err, static_cast<uint64_t>(limit_us) * 1000u, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
 int pkv_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* pkv_status_string(int status) {

@@ -68,6 +68,9 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
 
 cudaError_t launch_prefill(const AttnParams& p, int num_sms,
                            cudaStream_t stream);
+
+cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns,
+                                         cudaStream_t stream);
 bool prefill_supported(int head_size, int head_size_v, int dtype);
 
 }  // namespace pkv

@@ -55,10 +55,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // soon as another role has given up (the shared abort word), it records
 // PKV_EDEV_TIMEOUT in the device error word and returns false.  No wait in
 // the kernel is unbounded.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag, int* err,
-                                          bool honor_abort = true) {
-  constexpr uint64_t limit_ns = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, int* err,
+                                              uint64_t limit_ns, bool honor_abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -72,6 +71,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag, int* err,
+                                          bool honor_abort = true) {
+  return mbar_wait_for(bar, parity, abort_flag, err, 2000000000ull /* 2 s */, honor_abort);
 }
 
 // ------------------------------------------------------------------ TMA --
