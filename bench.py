@@ -206,12 +206,17 @@ def prefill_flops(w) -> float:
 # ----------------------------------------------------------- GPU arm ----
 
 class Flusher:
+    """Evicts L2 between timed launches: writes a buffer larger than L2 and
+    then reads it back, so that L2 holds clean lines of the flush buffer (no
+    write-back of flush data lands inside the next timed launch)."""
     def __init__(self, device):
         self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32,
                                device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
 
     def __call__(self):
         self.buf.fill_(1.0)
+        torch.sum(self.buf, dim=0, out=self.sink)
 
 
 def time_launches(fn, reps, warmup, flush=None):
