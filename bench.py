@@ -220,8 +220,9 @@ class Flusher:
 
 
 def time_launches(fn, reps, warmup, flush=None):
-    """Mean device time (ms) of fn() over reps launches, events on the current
-    stream, L2 flushed between launches when a flusher is given."""
+    """Median device time (ms) of fn() over reps launches (and the minimum),
+    events on the current stream, L2 flushed between launches when a flusher
+    is given."""
     for _ in range(warmup):
         fn()
     ts = []
@@ -235,7 +236,7 @@ def time_launches(fn, reps, warmup, flush=None):
         e1.record()
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))
-    return statistics.mean(ts), min(ts)
+    return statistics.median(ts), min(ts)
 
 
 def gpu_arm(args, ws, rank, local):
@@ -588,7 +589,7 @@ def main(argv=None):
     ap.add_argument("--only", choices=["prefill", "verify", "mla", "decode"],
                     help="run one sub-measurement alone (for profiling)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
-    ap.add_argument("--sub-reps", type=int, default=10)
+    ap.add_argument("--sub-reps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=30.0)
     args = ap.parse_args(argv)

@@ -215,7 +215,7 @@ int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
 
 /*
  * pkv_decode_suggest_splits -- a split count for the decode launch on the
- * current device: one work unit per SM for a single sequence; for a batch
+ * current device: two work units per SM for a single sequence; for a batch
  * two to four per SM, preferring a unit count that divides evenly over the
  * SMs (a unit covers four KV heads when num_kv_heads is a multiple of 4, else
  * one); for sequences of up to max_seq_len keys, capped so that every segment

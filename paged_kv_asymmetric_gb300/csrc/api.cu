@@ -320,12 +320,12 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
   const int64_t head_units = num_kv_heads % 4 == 0 ? num_kv_heads / 4 : num_kv_heads;
   const int64_t units = static_cast<int64_t>(num_seqs) * head_units *
                         ((max_query_len * G + 15) / 16);
-  // One unit per SM for a single sequence (its units are all alike).  For a
-  // batch at least two per SM, and among up to twice that many splits the
-  // count that would leave the fewest SMs idle at the end if the units were
-  // alike (ceil(n / sms) * sms / n), taking more splits only for a gain of
-  // more than 2 %.
-  int64_t s = (sms + units - 1) / units;
+  // Two units per SM for a single sequence (its units are all alike; some
+  // decode shapes run two CTAs per SM).  For a batch at least two per SM, and
+  // among up to twice that many splits the count that would leave the fewest
+  // SMs idle at the end if the units were alike (ceil(n / sms) * sms / n),
+  // taking more splits only for a gain of more than 2 %.
+  int64_t s = (2 * static_cast<int64_t>(sms) + units - 1) / units;
   if (num_seqs > 1) {
     const int64_t lo = (2 * static_cast<int64_t>(sms) + units - 1) / units;
     s = lo;

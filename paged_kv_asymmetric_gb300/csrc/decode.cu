@@ -62,8 +62,9 @@ namespace pkv {
 namespace {
 
 template <int DK_, int DV_, bool FP8_, int HPC_, int WG_, int NG_, int KPC_,
-          int NSLOT_, int NQ_, int SPAN_, bool NARROW_ = false>
+          int NSLOT_, int NQ_, int SPAN_, bool NARROW_ = false, int CTAS_ = 1>
 struct DecodeCfg {
+  static constexpr int CTAS = CTAS_;  // CTAs per SM
   static constexpr int DK = DK_, DV = DV_, HPC = HPC_, WG = WG_, NG = NG_;
   static constexpr int KPC = KPC_, NSLOT = NSLOT_, NQ = NQ_, SPAN = SPAN_;
   // narrow: a head's rows fit in 8 and the MMAs run transposed (S^T = K Q^T)
@@ -99,8 +100,11 @@ struct DecodeCfg {
   static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
   static constexpr int DESC_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int DESC_BYTES = 64 + MAXP * 4;  // descriptor + page ids
+  // Descriptor slots: two at least, so that staging unit n+1 (while unit n
+  // is issued from its page list) never overwrites unit n's.
+  static constexpr int ND = NQ > 2 ? NQ : 2;
   static constexpr int MAXSORT = 128;  // sequences ranked by length, at most
-  static constexpr int ORDER_OFF = DESC_OFF + NQ * DESC_BYTES;
+  static constexpr int ORDER_OFF = DESC_OFF + ND * DESC_BYTES;
   static constexpr int MERGE_OFF = ORDER_OFF + MAXSORT * 4;
   // every chunk class's (O, max, sum) per head and row, combined by all
   static constexpr int MROW = DVP + 2;
@@ -115,7 +119,7 @@ struct DecodeCfg {
   static_assert(DV % WG == 0 && DVS % (FP8 ? 128 : 16) == 0, "V slices");
   static_assert(QCH % 8 == 0, "Q rows in whole 128-byte groups");
   static_assert(KPC % 16 == 0 && KPC <= 256, "keys per chunk");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM * CTAS <= 227 * 1024, "shared memory budget");
   static_assert(NSLOT % NG == 0, "each ring slot belongs to one chunk class");
   static_assert(NGRP + 2 <= 15, "named barrier ids");
   static_assert(!NARROW || (!FP8 && NG == 1 && KSTEPS % WG == 0 && KSW % 2 == 0 &&
@@ -241,7 +245,7 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, i
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, C::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p,
                   int head_boxes) {
   extern __shared__ uint8_t smem_raw[];
@@ -398,9 +402,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int np = min(un.npages, C::MAXP);
         const int32_t* bt = p.block_table +
                             static_cast<int64_t>(un.b) * p.max_blocks_per_seq + un.page_lo;
-        const uint32_t pdst = sbase + C::DESC_OFF + qslot * C::DESC_BYTES + 64;
+        const uint32_t dslot = qs_n % C::ND;
+        const uint32_t pdst = sbase + C::DESC_OFF + dslot * C::DESC_BYTES + 64;
         for (int i = lane; i < np; i += 32) cp_async_4(pdst + 4 * i, bt + i);
-        if (lane == 0) *desc_of(qslot) = un;
+        if (lane == 0) *desc_of(dslot) = un;
         cp_async_commit();
         ++qs_n;
         return;
@@ -414,8 +419,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       cp_async_wait<0>();  // this unit's rows and page ids (staged last)
       __syncwarp();
       if (lane == 0) tc5::mbar_arrive(q_full(qslot));
-      const Unit un = *desc_of(qslot);
-      const int* pages = pages_of(qslot);
+      const Unit un = *desc_of(qi_n % C::ND);
+      const int* pages = pages_of(qi_n % C::ND);
       const int32_t* bt = p.block_table + static_cast<int64_t>(un.b) * p.max_blocks_per_seq;
       const int k_stage = min(un.nch, NSLOT) - 1;  // stage the next unit after this chunk
       for (int k = 0; k < un.nch; ++k) {
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) {
         w = tc5::mbar_wait(q_empty(qslot), ((qs_n / C::NQ) & 1u) ^ 1u, abort_flag, p.err);
         if (w) {
-          desc_of(qslot)->nch = -1;
+          desc_of(qs_n % C::ND)->nch = -1;
           tc5::mbar_arrive(q_full(qslot));
         }
       }
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       } else {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       }
-      const Unit un = *desc_of(qslot);
+      const Unit un = *desc_of(qc % C::ND);
       if (un.nch < 0) break;
       const int kvh = un.hb * HPC + hg;
       const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES + hg * C::QH_BYTES;
@@ -729,7 +734,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       } else {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       }
-      const Unit un = *desc_of(qslot);
+      const Unit un = *desc_of(qc % C::ND);
       if (un.nch < 0) break;
       const int kvh = un.hb * HPC + hg;  // this group's KV head
       const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES + hg * C::QH_BYTES;
@@ -1111,7 +1116,8 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
   const int64_t RG = (static_cast<int64_t>(p.max_query_len) * p.group + 15) / 16;
   const int64_t units = static_cast<int64_t>(p.num_splits) * p.num_seqs *
                         (p.num_kv_heads / C::HPC) * RG;
-  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+  const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
+  const int grid = static_cast<int>(units < slots ? units : slots);
   decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, p, head_boxes);
   return cudaGetLastError();
 }
@@ -1128,7 +1134,7 @@ using CfgBf16_192x1 = DecodeCfg<192, 128, false, 1, 1, 6, 16, 12, 4, 320>;
 // 64), six chunk classes.
 using CfgFp8_192 = DecodeCfg<192, 128, true, 1, 1, 6, 64, 6, 2, 320>;
 // MLA 576 / 512: one latent head, 32 (bf16) or 64 (fp8) keys per chunk.
-using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 4, 2, 576>;
+using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 2, 1, 576, false, 2>;
 using CfgFp8_576 = DecodeCfg<576, 512, true, 1, 4, 1, 64, 4, 2, 576>;
 
 }  // namespace
