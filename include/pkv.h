@@ -196,6 +196,50 @@ int pkv_paged_attn_decode(const void *q, int num_q_heads, int num_tokens,
                           float *partial_lse, pkv_stream_t stream);
 
 /*
+ * pkv_decode_workspace_bytes -- size of the workspace that
+ * pkv_paged_attn_decode_fused needs for these sizes: one 32-bit counter per
+ * (sequence, KV head, 16-row group of the head's q_len * G rows).  Returns
+ * 0 for invalid sizes.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int max_query_len);
+
+/*
+ * pkv_paged_attn_decode_fused -- pkv_paged_attn_decode and
+ * pkv_splitkv_reduce in one launch (the fused split merge ranked next in
+ * the scope of this library; the pages merge in a second stage, vLLM PR
+ * #50371 discussion, "both stages").  Every work unit writes its segment's
+ * partials as pkv_paged_attn_decode does, then counts itself done in the
+ * workspace; the last unit of each (sequence, KV-head block, row group) to
+ * finish merges all segments of its rows as pkv_splitkv_reduce does (0 and
+ * lse -inf for a row with no visible key) into out (bf16 [num_tokens]
+ * [num_q_heads][head_size_v]) and lse_out (float32 [num_tokens]
+ * [num_q_heads], or NULL), and resets its counter.
+ * workspace: device memory of at least pkv_decode_workspace_bytes(...)
+ * (workspace_bytes gives its size), zero-filled by the caller before its
+ * first use; every call leaves it zero again, so it can be reused without
+ * clearing (after a call that ended with a device error -- see
+ * pkv_get_device_error -- it must be zero-filled again).  Calls that overlap
+ * in time must not share a workspace.
+ * partial_o / partial_lse are scratch here (same shapes as in
+ * pkv_paged_attn_decode).  For num_splits > 32 the merge runs as a second
+ * launch on the same stream (same results, workspace untouched).  Other
+ * arguments, sizes and status codes as in pkv_paged_attn_decode; PKV_EINVAL
+ * also for a missing or too small workspace or a null out.
+ */
+int pkv_paged_attn_decode_fused(const void *q, int num_q_heads, int num_tokens,
+                                const void *cache, const pkv_cache_desc *d,
+                                const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *seq_lens,
+                                const int32_t *query_start_loc, int num_seqs,
+                                int max_query_len, float softmax_scale,
+                                const float *k_scale, const float *v_scale,
+                                int num_splits, float *partial_o,
+                                float *partial_lse, void *workspace,
+                                size_t workspace_bytes, void *out, float *lse_out,
+                                pkv_stream_t stream);
+
+/*
  * pkv_splitkv_reduce -- the split-KV merge (MiMo model card, "What the
  * kernels do" and "Update 2026-10-01").
  *

@@ -33,7 +33,7 @@ SCALE_NONE, SCALE_TENSOR, SCALE_HEAD = 0, 1, 2
 
 EXPORTED = (
     "pkv_kv_cache_write", "pkv_paged_attn_prefill", "pkv_paged_attn_decode",
-    "pkv_splitkv_reduce", "pkv_decode_suggest_splits", "pkv_supports",
+    "pkv_paged_attn_decode_fused", "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_decode_suggest_splits", "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
 )
@@ -91,6 +91,11 @@ def _lib():
                                                F, P, P, P, P]
         lib.pkv_paged_attn_decode.argtypes = [P, I, I, P, D, P, I, P, P, I, I,
                                               F, P, P, I, P, P, P]
+        lib.pkv_paged_attn_decode_fused.argtypes = [P, I, I, P, D, P, I, P, P, I,
+                                                    I, F, P, P, I, P, P, P,
+                                                    ctypes.c_size_t, P, P, P]
+        lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I]
+        lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_splitkv_reduce.argtypes = [P, P, I, I, I, P, P, P]
         lib.pkv_decode_suggest_splits.argtypes = [I, I, I, I, I, I]
         lib.pkv_supports.argtypes = [I, I, I]
@@ -100,7 +105,7 @@ def _lib():
         lib.pkv_status_string.argtypes = [I]
         lib.pkv_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("pkv_status_string",):
+            if name not in ("pkv_status_string", "pkv_decode_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _handle = lib
         return lib
@@ -208,6 +213,42 @@ def paged_attn_decode(q, cache: Cache, block_table, seq_lens,
         float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(num_splits),
         _ptr(partial_o), _ptr(partial_lse), _stream(stream)))
     return partial_o, partial_lse
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_query_len) -> int:
+    return int(_lib().pkv_decode_workspace_bytes(int(num_seqs), int(num_q_heads),
+                                                 int(num_kv_heads), int(max_query_len)))
+
+
+def paged_attn_decode_fused(q, cache: Cache, block_table, seq_lens,
+                            query_start_loc, softmax_scale, max_query_len,
+                            num_splits, workspace, out=None, lse_out=None,
+                            partial_o=None, partial_lse=None, k_scale=None,
+                            v_scale=None, stream=None):
+    """Decode and split merge in one launch (pkv_paged_attn_decode_fused).
+    `workspace`: a zero-filled int32 (or byte) CUDA tensor of at least
+    decode_workspace_bytes(...) bytes, left zero by every call.  Returns
+    (out [T, Hq, dv] bf16, lse_out or None)."""
+    _attn_common(q, block_table, seq_lens, query_start_loc)
+    T, Hq, _ = q.shape
+    dv = cache.desc.head_size_v
+    if partial_o is None:
+        partial_o = torch.empty(num_splits, T, Hq, dv, dtype=torch.float32,
+                                device=q.device)
+    if partial_lse is None:
+        partial_lse = torch.empty(num_splits, T, Hq, dtype=torch.float32,
+                                  device=q.device)
+    if out is None:
+        out = torch.empty(T, Hq, dv, dtype=torch.bfloat16, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pkv_paged_attn_decode_fused", _lib().pkv_paged_attn_decode_fused(
+        _ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+        _ptr(query_start_loc), int(seq_lens.shape[0]), int(max_query_len),
+        float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(num_splits),
+        _ptr(partial_o), _ptr(partial_lse), _ptr(workspace), ws_bytes,
+        _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
 
 
 def splitkv_reduce(partial_o, partial_lse, out=None, lse_out=None,

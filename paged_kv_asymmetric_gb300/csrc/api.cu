@@ -226,15 +226,18 @@ int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }
 
-int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
-                          const void* cache, const pkv_cache_desc* d,
-                          const int32_t* block_table, int max_blocks_per_seq,
-                          const int32_t* seq_lens,
-                          const int32_t* query_start_loc, int num_seqs,
-                          int max_query_len, float softmax_scale,
-                          const float* k_scale, const float* v_scale,
-                          int num_splits, float* partial_o, float* partial_lse,
-                          pkv_stream_t stream) {
+namespace {
+
+// Checks of pkv_paged_attn_decode and its fused form, and the kernel
+// parameters they share.  `launch` is false when there is nothing to do.
+int decode_prepare(const void* q, int num_q_heads, int num_tokens, const void* cache,
+                   const pkv_cache_desc* d, const int32_t* block_table,
+                   int max_blocks_per_seq, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int num_seqs, int max_query_len,
+                   float softmax_scale, const float* k_scale, const float* v_scale,
+                   int num_splits, float* partial_o, float* partial_lse,
+                   pkv::AttnParams* p, int* sms, bool* launch) {
+  *launch = false;
   int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
                              max_blocks_per_seq, seq_lens, query_start_loc,
                              num_seqs, softmax_scale, k_scale, v_scale);
@@ -269,19 +272,95 @@ int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
   if (!(d->block_size % 16 == 0 || d->block_size == 8)) return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
   int* err = nullptr;
-  int sms = 0;
-  rc = device_info(&err, &sms);
+  rc = device_info(&err, sms);
   if (rc != PKV_OK) return rc;
-  pkv::AttnParams p = make_params(q, num_q_heads, num_tokens, cache, d,
-                                  block_table, max_blocks_per_seq, seq_lens,
-                                  query_start_loc, num_seqs, softmax_scale,
-                                  k_scale, v_scale, err);
-  p.max_query_len = max_query_len;
-  p.num_splits = num_splits;
-  p.partial_o = partial_o;
-  p.partial_lse = partial_lse;
+  *p = make_params(q, num_q_heads, num_tokens, cache, d, block_table,
+                   max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                   softmax_scale, k_scale, v_scale, err);
+  p->max_query_len = max_query_len;
+  p->num_splits = num_splits;
+  p->partial_o = partial_o;
+  p->partial_lse = partial_lse;
+  *launch = true;
+  return PKV_OK;
+}
+
+}  // namespace
+
+int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
+                          const void* cache, const pkv_cache_desc* d,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens,
+                          const int32_t* query_start_loc, int num_seqs,
+                          int max_query_len, float softmax_scale,
+                          const float* k_scale, const float* v_scale,
+                          int num_splits, float* partial_o, float* partial_lse,
+                          pkv_stream_t stream) {
+  pkv::AttnParams p{};
+  int sms = 0;
+  bool launch = false;
+  const int rc = decode_prepare(q, num_q_heads, num_tokens, cache, d, block_table,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, softmax_scale, k_scale, v_scale, num_splits,
+                                partial_o, partial_lse, &p, &sms, &launch);
+  if (rc != PKV_OK || !launch) return rc;
   cudaError_t e = pkv::launch_decode(p, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int max_query_len) {
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_query_len < 1 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int64_t G = num_q_heads / num_kv_heads;
+  const int64_t rg = (static_cast<int64_t>(max_query_len) * G + 15) / 16;
+  return static_cast<size_t>(num_seqs) * num_kv_heads * rg * sizeof(int);
+}
+
+int pkv_paged_attn_decode_fused(const void* q, int num_q_heads, int num_tokens,
+                                const void* cache, const pkv_cache_desc* d,
+                                const int32_t* block_table, int max_blocks_per_seq,
+                                const int32_t* seq_lens,
+                                const int32_t* query_start_loc, int num_seqs,
+                                int max_query_len, float softmax_scale,
+                                const float* k_scale, const float* v_scale,
+                                int num_splits, float* partial_o, float* partial_lse,
+                                void* workspace, size_t workspace_bytes, void* out,
+                                float* lse_out, pkv_stream_t stream) {
+  pkv::AttnParams p{};
+  int sms = 0;
+  bool launch = false;
+  int rc = decode_prepare(q, num_q_heads, num_tokens, cache, d, block_table,
+                          max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                          max_query_len, softmax_scale, k_scale, v_scale, num_splits,
+                          partial_o, partial_lse, &p, &sms, &launch);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens > 0 && out == nullptr) return PKV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return PKV_EINVAL;
+  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, d->num_kv_heads,
+                                                 max_query_len);
+  if (num_tokens > 0 && (workspace == nullptr || workspace_bytes < need ||
+                         (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
+    return PKV_EINVAL;
+  if (!launch) return PKV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse_out = lse_out;
+  if (num_splits <= pkv::kFusedMaxSplits) {
+    p.counters = static_cast<int*>(workspace);
+    p.fused = 1;
+    cudaError_t e = pkv::launch_decode(p, sms, s);
+    if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+  }
+  cudaError_t e = pkv::launch_decode(p, sms, s);
+  if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+  if (e == cudaSuccess)
+    e = pkv::launch_splitkv_reduce(partial_o, partial_lse, num_splits,
+                                   num_tokens * num_q_heads, d->head_size_v,
+                                   p.out, lse_out, s);
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }
 

@@ -112,7 +112,14 @@ struct DecodeCfg {
   static constexpr int SBUF_OFF = MERGE_OFF + MERGE;
   static constexpr int SBUF_LANE = NARROW ? 4 : 8;  // partial scores per lane
   static constexpr int SBUF = WG > 1 ? NGRP * 2 * WG * 32 * SBUF_LANE * 4 : 0;
-  static constexpr int BAR_OFF = SBUF_OFF + SBUF;
+  // Fused merge: per (head, row) weights of up to kFusedMaxSplits splits and
+  // a flag; it reuses the score-exchange or class-merge buffer (idle at the
+  // end of a unit) when one is large enough.
+  static constexpr int WBUF = HPC * 16 * kFusedMaxSplits * 4 + 16;
+  static constexpr int WBUF_OFF = SBUF >= WBUF ? SBUF_OFF : MERGE >= WBUF ? MERGE_OFF
+                                                                          : SBUF_OFF + SBUF;
+  static constexpr int BAR_OFF = (SBUF >= WBUF || MERGE >= WBUF) ? SBUF_OFF + SBUF
+                                                                 : SBUF_OFF + SBUF + WBUF;
   static constexpr int NBAR = 2 * NSLOT + 2 * NQ;
   static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
   static_assert(DK % 64 == 0, "K in 64-column units");
@@ -244,6 +251,91 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, i
   un.pad0 = un.pad1 = 0;
 }
 
+// The end of a unit in the fused decode, run by every consumer thread of
+// the CTA (ctid = its index among them) once the unit's partials are
+// written.  The unit counts itself done; the last unit of its (sequence,
+// KV-head block, row group) merges the segments of its rows as
+// pkv_splitkv_reduce does and puts the counter back to zero.  Ordering: a
+// barrier, then one thread's fence before its atomic, publishes the CTA's
+// partial writes; the last unit fences after its atomic and reads the
+// partials with L1-bypassing loads.
+template <class C>
+__device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un, int HB,
+                                             int RG, uint8_t* smem, int ctid) {
+  constexpr int NT = 32 * C::NCW;
+  float* wb = reinterpret_cast<float*>(smem + C::WBUF_OFF);
+  volatile int* flag =
+      reinterpret_cast<volatile int*>(smem + C::WBUF_OFF + C::HPC * 16 * kFusedMaxSplits * 4);
+  named_barrier(1, NT);  // the unit's partials are written
+  if (ctid == 0) {
+    __threadfence();
+    const int key = (un.b * HB + un.hb) * RG + un.row0 / 16;
+    const int last = atomicAdd(p.counters + key, 1) == p.num_splits - 1;
+    if (last) {
+      p.counters[key] = 0;  // zero again for the next call
+      __threadfence();
+    }
+    *flag = last;
+  }
+  named_barrier(1, NT);
+  if (!*flag) return;
+  const int S = p.num_splits;
+  const int64_t TH = static_cast<int64_t>(p.num_tokens) * p.num_q_heads;
+  const int G = p.group;
+  const int nr = C::HPC * un.nrows;
+  auto row_of = [&](int h, int r) {
+    const int rr = un.row0 + r;
+    return (static_cast<int64_t>(un.qs) + rr / G) * p.num_q_heads + (un.hb * C::HPC + h) * G +
+           rr % G;
+  };
+  // per row: the segments' weights exp(lse_s - M) / sum, and the merged lse
+  for (int i = ctid; i < nr; i += NT) {
+    const int h = i / un.nrows, r = i - h * un.nrows;
+    const int64_t row = row_of(h, r);
+    float* w = wb + i * kFusedMaxSplits;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(p.partial_lse + s * TH + row));
+    if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
+      for (int s = 0; s < S; ++s) w[s] = 0.f;
+      if (p.lse_out != nullptr) p.lse_out[row] = -INFINITY;
+      continue;
+    }
+    const float Ml2 = M * kLog2e;
+    float W = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float x = __ldcg(p.partial_lse + s * TH + row);
+      const float e = x == -INFINITY ? 0.f : fast_exp2(fmaf(x, kLog2e, -Ml2));
+      w[s] = e;
+      W += e;
+    }
+    const float inv = 1.f / W;
+    for (int s = 0; s < S; ++s) w[s] *= inv;
+    if (p.lse_out != nullptr) p.lse_out[row] = M + fast_log2(W) * kLn2;
+  }
+  named_barrier(1, NT);
+  constexpr int DV4 = C::DV / 4;
+  for (int i = ctid; i < nr * DV4; i += NT) {
+    const int hr = i / DV4, c4 = i - hr * DV4;
+    const int h = hr / un.nrows, r = hr - h * un.nrows;
+    const int64_t row = row_of(h, r);
+    const float* w = wb + hr * kFusedMaxSplits;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float ws = w[s];
+      if (ws == 0.f) continue;  // an empty segment's partial is not read
+      const float4 v =
+          __ldcg(reinterpret_cast<const float4*>(p.partial_o + (s * TH + row) * C::DV) + c4);
+      acc.x = fmaf(ws, v.x, acc.x);
+      acc.y = fmaf(ws, v.y, acc.y);
+      acc.z = fmaf(ws, v.z, acc.z);
+      acc.w = fmaf(ws, v.w, acc.w);
+    }
+    *reinterpret_cast<uint2*>(p.out + row * C::DV + 4 * c4) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+  named_barrier(1, NT);  // the weights are read before the buffer is reused
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p,
@@ -370,7 +462,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         ++pos;
         meta_load(pos);  // the next unit's metadata is in flight meanwhile
         if (un.nrows == 0) continue;
-        if (un.nch == 0) {  // no key of this segment is visible to any row
+        if (un.nch == 0 && !p.fused) {  // no key of this segment is visible to any row
           for (int i = lane; i < HPC * un.nrows; i += 32) {
             const int h = i / un.nrows, r = i - h * un.nrows;
             const int rr = un.row0 + r;
@@ -468,6 +560,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         ++gc;
         if (k == k_stage && alive) stage_next();
       }
+      // a unit without chunks (an empty segment staged for the fused merge)
+      // stages the next one here
+      if (alive && qs_n == qi_n + 1) stage_next();
       ++qi_n;
     }
     if (alive) {  // end marker for the consumers
@@ -516,8 +611,12 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     for (;;) {
       const uint32_t qslot = qc % C::NQ;
       wait_all(q_full(qslot), (qc / C::NQ) & 1u);
-      // the warps of a group take the same decision to stop after a timeout
-      if constexpr (WG > 1) {
+      // the warps that meet at named barriers take the same decision to stop
+      // after a timeout: all consumer warps when units end in the fused
+      // merge, else the warps of a group
+      if (p.fused) {
+        if (barrier_or(15, 32 * C::NCW, *abort_flag != 0)) break;
+      } else if constexpr (WG > 1) {
         if (barrier_or(2 + grp, 32 * WG, *abort_flag != 0)) break;
       } else {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -699,6 +798,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           p.partial_lse[orow] =
               l_run[j] > 0.f ? (m_run[j] + fast_log2(l_run[j])) * kLn2 : -INFINITY;
       }
+      if (p.fused) fused_finish<C>(p, un, us.HB, us.RG, smem, threadIdx.x - 32);
     }
   } else {
     // ------------------------------------------------ consumer warps ----
@@ -725,9 +825,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
       const uint32_t qslot = qc % C::NQ;
       wait_all(q_full(qslot), (qc / C::NQ) & 1u);
       // The warps that meet at named barriers take the same decision to stop
-      // after a timeout: all consumer warps when the classes merge, else the
-      // warps of one group.
-      if constexpr (NG > 1) {
+      // after a timeout: all consumer warps when the classes merge or units
+      // end in the fused merge, else the warps of one group.
+      if (NG > 1 || p.fused) {
         if (barrier_or(15, 32 * C::NCW, *abort_flag != 0)) break;
       } else if constexpr (WG > 1) {
         if (barrier_or(2 + grp, 32 * WG, *abort_flag != 0)) break;
@@ -1091,6 +1191,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
                 l_run[kr] > 0.f ? (m_run[kr] + fast_log2(l_run[kr])) * kLn2 : -INFINITY;
         }
       }
+      if (p.fused) fused_finish<C>(p, un, us.HB, us.RG, smem, threadIdx.x - 32);
     }
   }
 }

@@ -48,10 +48,19 @@ struct AttnParams {
   int num_splits;
   float* partial_o;            // [S][T][Hq][dv]
   float* partial_lse;          // [S][T][Hq]
-  // prefill
+  // prefill, and the fused decode's merged output
   __nv_bfloat16* out;          // [T][Hq][dv]
   int* err;
+  // fused decode: counters of finished units per (sequence, KV-head block,
+  // row group), the merged lse (nullable), and whether to merge in-kernel
+  int* counters;
+  float* lse_out;
+  int fused;
 };
+
+// The fused decode merges in-kernel up to this many splits (its per-row
+// weights live in shared memory); beyond, the merge is a second launch.
+constexpr int kFusedMaxSplits = 32;
 
 cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
                                cudaStream_t stream);
