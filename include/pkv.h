@@ -240,6 +240,37 @@ int pkv_paged_attn_decode_fused(const void *q, int num_q_heads, int num_tokens,
                                 pkv_stream_t stream);
 
 /*
+ * pkv_paged_attn_decode_fused_noalloc -- pkv_paged_attn_decode_fused
+ * without a caller workspace.  The pages have no counterpart: this entry
+ * exists for callers that have no device allocator at hand.  Its counters
+ * live in a fixed array of 65536 32-bit counters (256 KB) in this library's
+ * own device memory, one array per device, whose address is looked up once
+ * per device; nothing is allocated.  After every argument has been checked,
+ * each call zero-fills, on `stream`, the counters it is about to use (so a
+ * call after a device error needs no clearing), then launches as
+ * pkv_paged_attn_decode_fused does.  All calls on a device share that one
+ * array: calls that overlap in time (on different streams or host threads)
+ * race on it and give wrong results, so serialise them.
+ * PKV_EINVAL also when pkv_decode_workspace_bytes(num_seqs, num_q_heads,
+ * d->num_kv_heads, max_query_len) exceeds 256 KB (more than 65536 counters);
+ * other arguments, results and status codes as in
+ * pkv_paged_attn_decode_fused.
+ */
+int pkv_paged_attn_decode_fused_noalloc(const void *q, int num_q_heads,
+                                        int num_tokens, const void *cache,
+                                        const pkv_cache_desc *d,
+                                        const int32_t *block_table,
+                                        int max_blocks_per_seq,
+                                        const int32_t *seq_lens,
+                                        const int32_t *query_start_loc,
+                                        int num_seqs, int max_query_len,
+                                        float softmax_scale, const float *k_scale,
+                                        const float *v_scale, int num_splits,
+                                        float *partial_o, float *partial_lse,
+                                        void *out, float *lse_out,
+                                        pkv_stream_t stream);
+
+/*
  * pkv_splitkv_reduce -- the split-KV merge (MiMo model card, "What the
  * kernels do" and "Update 2026-10-01").
  *

@@ -33,7 +33,9 @@ SCALE_NONE, SCALE_TENSOR, SCALE_HEAD = 0, 1, 2
 
 EXPORTED = (
     "pkv_kv_cache_write", "pkv_paged_attn_prefill", "pkv_paged_attn_decode",
-    "pkv_paged_attn_decode_fused", "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_decode_suggest_splits", "pkv_supports",
+    "pkv_paged_attn_decode_fused", "pkv_paged_attn_decode_fused_noalloc",
+    "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_decode_suggest_splits",
+    "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
 )
@@ -94,6 +96,8 @@ def _lib():
         lib.pkv_paged_attn_decode_fused.argtypes = [P, I, I, P, D, P, I, P, P, I,
                                                     I, F, P, P, I, P, P, P,
                                                     ctypes.c_size_t, P, P, P]
+        lib.pkv_paged_attn_decode_fused_noalloc.argtypes = [
+            P, I, I, P, D, P, I, P, P, I, I, F, P, P, I, P, P, P, P, P]
         lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_splitkv_reduce.argtypes = [P, P, I, I, I, P, P, P]
@@ -248,6 +252,40 @@ def paged_attn_decode_fused(q, cache: Cache, block_table, seq_lens,
         float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(num_splits),
         _ptr(partial_o), _ptr(partial_lse), _ptr(workspace), ws_bytes,
         _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
+
+
+NOALLOC_MAX_COUNTERS = 65536
+
+
+def paged_attn_decode_fused_noalloc(q, cache: Cache, block_table, seq_lens,
+                                    query_start_loc, softmax_scale, max_query_len,
+                                    num_splits, out=None, lse_out=None,
+                                    partial_o=None, partial_lse=None,
+                                    k_scale=None, v_scale=None, stream=None):
+    """paged_attn_decode_fused with the library's own fixed counter array
+    (pkv_paged_attn_decode_fused_noalloc): no workspace argument, at most
+    NOALLOC_MAX_COUNTERS counters, and calls that overlap in time race.
+    Returns (out [T, Hq, dv] bf16, lse_out or None)."""
+    _attn_common(q, block_table, seq_lens, query_start_loc)
+    T, Hq, _ = q.shape
+    dv = cache.desc.head_size_v
+    if partial_o is None:
+        partial_o = torch.empty(num_splits, T, Hq, dv, dtype=torch.float32,
+                                device=q.device)
+    if partial_lse is None:
+        partial_lse = torch.empty(num_splits, T, Hq, dtype=torch.float32,
+                                  device=q.device)
+    if out is None:
+        out = torch.empty(T, Hq, dv, dtype=torch.bfloat16, device=q.device)
+    _check("pkv_paged_attn_decode_fused_noalloc",
+           _lib().pkv_paged_attn_decode_fused_noalloc(
+               _ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
+               _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+               _ptr(query_start_loc), int(seq_lens.shape[0]), int(max_query_len),
+               float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(num_splits),
+               _ptr(partial_o), _ptr(partial_lse), _ptr(out), _ptr(lse_out),
+               _stream(stream)))
     return out, lse_out
 
 

@@ -23,6 +23,13 @@ std::mutex g_dev_mu;
 int* g_err_ptr[kMaxDevices] = {nullptr};
 int g_num_sms[kMaxDevices] = {0};
 
+// Counters of pkv_paged_attn_decode_fused_noalloc: a fixed array in the
+// library's device image instead of a caller workspace (one per device; all
+// calls on a device share it).
+constexpr int kNoAllocCounters = 65536;
+static __device__ __align__(256) int g_noalloc_counters[kNoAllocCounters];
+int* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
 int fail_cuda(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
   return PKV_ECUDA;
@@ -319,16 +326,18 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
   return static_cast<size_t>(num_seqs) * num_kv_heads * rg * sizeof(int);
 }
 
-int pkv_paged_attn_decode_fused(const void* q, int num_q_heads, int num_tokens,
-                                const void* cache, const pkv_cache_desc* d,
-                                const int32_t* block_table, int max_blocks_per_seq,
-                                const int32_t* seq_lens,
-                                const int32_t* query_start_loc, int num_seqs,
-                                int max_query_len, float softmax_scale,
-                                const float* k_scale, const float* v_scale,
-                                int num_splits, float* partial_o, float* partial_lse,
-                                void* workspace, size_t workspace_bytes, void* out,
-                                float* lse_out, pkv_stream_t stream) {
+namespace {
+
+// The fused decode; with `clear`, the counters it uses are zeroed on the
+// stream first (after every argument has been checked).
+int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void* cache,
+                      const pkv_cache_desc* d, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* seq_lens,
+                      const int32_t* query_start_loc, int num_seqs, int max_query_len,
+                      float softmax_scale, const float* k_scale, const float* v_scale,
+                      int num_splits, float* partial_o, float* partial_lse, void* workspace,
+                      size_t workspace_bytes, void* out, float* lse_out, pkv_stream_t stream,
+                      bool clear) {
   pkv::AttnParams p{};
   int sms = 0;
   bool launch = false;
@@ -346,6 +355,10 @@ int pkv_paged_attn_decode_fused(const void* q, int num_q_heads, int num_tokens,
     return PKV_EINVAL;
   if (!launch) return PKV_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (clear && num_splits <= pkv::kFusedMaxSplits) {
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse_out = lse_out;
   if (num_splits <= pkv::kFusedMaxSplits) {
@@ -362,6 +375,63 @@ int pkv_paged_attn_decode_fused(const void* q, int num_q_heads, int num_tokens,
                                    num_tokens * num_q_heads, d->head_size_v,
                                    p.out, lse_out, s);
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+int pkv_paged_attn_decode_fused(const void* q, int num_q_heads, int num_tokens,
+                                const void* cache, const pkv_cache_desc* d,
+                                const int32_t* block_table, int max_blocks_per_seq,
+                                const int32_t* seq_lens,
+                                const int32_t* query_start_loc, int num_seqs,
+                                int max_query_len, float softmax_scale,
+                                const float* k_scale, const float* v_scale,
+                                int num_splits, float* partial_o, float* partial_lse,
+                                void* workspace, size_t workspace_bytes, void* out,
+                                float* lse_out, pkv_stream_t stream) {
+  return decode_fused_impl(q, num_q_heads, num_tokens, cache, d, block_table,
+                           max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                           max_query_len, softmax_scale, k_scale, v_scale, num_splits,
+                           partial_o, partial_lse, workspace, workspace_bytes, out, lse_out,
+                           stream, /*clear=*/false);
+}
+
+int pkv_paged_attn_decode_fused_noalloc(const void* q, int num_q_heads, int num_tokens,
+                                        const void* cache, const pkv_cache_desc* d,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* seq_lens,
+                                        const int32_t* query_start_loc, int num_seqs,
+                                        int max_query_len, float softmax_scale,
+                                        const float* k_scale, const float* v_scale,
+                                        int num_splits, float* partial_o,
+                                        float* partial_lse, void* out, float* lse_out,
+                                        pkv_stream_t stream) {
+  if (d == nullptr) return PKV_EINVAL;
+  // the sizes must fit the fixed counter array
+  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, d->num_kv_heads,
+                                                 max_query_len);
+  if (need > sizeof(int) * static_cast<size_t>(kNoAllocCounters)) return PKV_EINVAL;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return fail_cuda(cudaErrorInvalidDevice);
+  int* counters = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_counters);
+      if (e != cudaSuccess) return fail_cuda(e);
+      g_noalloc_ptr[dev] = static_cast<int*>(ptr);
+    }
+    counters = g_noalloc_ptr[dev];
+  }
+  return decode_fused_impl(q, num_q_heads, num_tokens, cache, d, block_table,
+                           max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                           max_query_len, softmax_scale, k_scale, v_scale, num_splits,
+                           partial_o, partial_lse, counters,
+                           sizeof(int) * static_cast<size_t>(kNoAllocCounters), out,
+                           lse_out, stream, /*clear=*/true);
 }
 
 int pkv_splitkv_reduce(const float* partial_o, const float* partial_lse,
