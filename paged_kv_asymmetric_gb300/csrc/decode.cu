@@ -62,9 +62,13 @@ namespace pkv {
 namespace {
 
 template <int DK_, int DV_, bool FP8_, int HPC_, int WG_, int NG_, int KPC_,
-          int NSLOT_, int NQ_, int SPAN_, bool NARROW_ = false, int CTAS_ = 1>
+          int NSLOT_, int NQ_, int SPAN_, bool NARROW_ = false, int CTAS_ = 1,
+          bool TC_ = false>
 struct DecodeCfg {
   static constexpr int CTAS = CTAS_;  // CTAs per SM
+  // tensor-core form (fp8 cache, one head, 128-key chunks): one MMA-issuing
+  // warp and four softmax warps, one key per thread; S^T and O^T in TMEM
+  static constexpr bool TC = TC_;
   static constexpr int DK = DK_, DV = DV_, HPC = HPC_, WG = WG_, NG = NG_;
   static constexpr int KPC = KPC_, NSLOT = NSLOT_, NQ = NQ_, SPAN = SPAN_;
   // narrow: a head's rows fit in 8 and the MMAs run transposed (S^T = K Q^T)
@@ -83,7 +87,13 @@ struct DecodeCfg {
   static constexpr int CB_STRIDE = HPC * CB_BYTES;
   static constexpr int SLOT_BYTES = NBOX * CB_STRIDE;
   static constexpr int NGRP = HPC * NG;                  // consumer groups
-  static constexpr int NCW = NGRP * WG;                  // consumer warps
+  static constexpr int SXW = TC ? 8 : 0;                 // softmax warps (TC)
+  static constexpr int NCW = TC ? SXW + 1 : NGRP * WG;   // consumer warps
+  // threads of the fused merge at the end of a unit
+  static constexpr int FIN_THREADS = TC ? 32 * SXW : 32 * NCW;
+  // arrivals that free a ring slot / a Q slot
+  static constexpr int SLOT_EMPTY_N = TC ? SXW + 1 : HPC * WG;
+  static constexpr int Q_EMPTY_N = TC ? SXW + 1 : NCW;
   static constexpr int THREADS = 32 * (1 + NCW);
   static constexpr int QCH = DK * 2 / 16;                // 16-byte Q pieces per row
   static constexpr int QH_BYTES = QROWS * DK * 2;        // one head's Q rows
@@ -97,7 +107,16 @@ struct DecodeCfg {
   static constexpr int NT = DVS / 8;
   static constexpr int DVP = DV + 4;
   static constexpr int RING_OFF = 0;
-  static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
+  // tensor-core form: V converted to f16 ([64-column slab][KPC keys][128 B],
+  // 128-byte swizzle), P^T in f16 ([64-key atom][16 rows][128 B]) twice, and
+  // Q as two E4M3 terms ([term][128-column atom][16 rows][128 B]) twice
+  static constexpr int V16_OFF = RING_OFF + NSLOT * SLOT_BYTES;
+  static constexpr int V16_BYTES = TC ? (DV / 64) * KPC * 128 : 0;
+  static constexpr int PT_OFF = V16_OFF + V16_BYTES;
+  static constexpr int PT_BYTES = TC ? (KPC / 64) * 16 * 128 : 0;
+  static constexpr int Q8_OFF = PT_OFF + 2 * PT_BYTES;
+  static constexpr int Q8_BYTES = TC ? 2 * ((DK + 127) / 128) * 16 * 128 : 0;
+  static constexpr int Q_OFF = Q8_OFF + 2 * Q8_BYTES;
   static constexpr int DESC_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int DESC_BYTES = 64 + MAXP * 4;  // descriptor + page ids
   // Descriptor slots: two at least, so that staging unit n+1 (while unit n
@@ -120,8 +139,14 @@ struct DecodeCfg {
                                                                           : SBUF_OFF + SBUF;
   static constexpr int BAR_OFF = (SBUF >= WBUF || MERGE >= WBUF) ? SBUF_OFF + SBUF
                                                                  : SBUF_OFF + SBUF + WBUF;
-  static constexpr int NBAR = 2 * NSLOT + 2 * NQ;
-  static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16 + 1024;
+  // tensor-core form: s_full[2], s_free[2], p_full[2], pv_done[2],
+  // q8_full[2], final; then scratch: per-row Q scales [2][16], the row
+  // reductions [4 warps][16], the row sums [16] and the TMEM address
+  static constexpr int NBAR_TC = TC ? 11 : 0;
+  static constexpr int NBAR = 2 * NSLOT + 2 * NQ + NBAR_TC;
+  static constexpr int TCS_OFF = BAR_OFF + NBAR * 8 + 16;
+  static constexpr int TCS_BYTES = TC ? (2 * 16 + 4 * 16 + 16 + 4) * 4 : 0;
+  static constexpr int SMEM = TCS_OFF + TCS_BYTES + 1024;
   static_assert(DK % 64 == 0, "K in 64-column units");
   static_assert(DV % WG == 0 && DVS % (FP8 ? 128 : 16) == 0, "V slices");
   static_assert(QCH % 8 == 0, "Q rows in whole 128-byte groups");
@@ -129,6 +154,9 @@ struct DecodeCfg {
   static_assert(SMEM * CTAS <= 227 * 1024, "shared memory budget");
   static_assert(NSLOT % NG == 0, "each ring slot belongs to one chunk class");
   static_assert(NGRP + 2 <= 15, "named barrier ids");
+  static_assert(!TC || (FP8 && HPC == 1 && NG == 1 && WG == 1 && KPC == 128 && DK == 192 &&
+                         DV == 128 && !NARROW && CTAS == 1),
+                "tensor-core form: fp8, one head, 128-key chunks, K 192 / V 128");
   static_assert(!NARROW || (!FP8 && NG == 1 && KSTEPS % WG == 0 && KSW % 2 == 0 &&
                              DVS % 16 == 0),
                 "narrow form: bf16, one chunk class, k-step pairs, 16-column V tiles");
@@ -262,7 +290,7 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, i
 template <class C>
 __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un, int HB,
                                              int RG, uint8_t* smem, int ctid) {
-  constexpr int NT = 32 * C::NCW;
+  constexpr int NT = C::FIN_THREADS;
   float* wb = reinterpret_cast<float*>(smem + C::WBUF_OFF);
   volatile int* flag =
       reinterpret_cast<volatile int*>(smem + C::WBUF_OFF + C::HPC * 16 * kFusedMaxSplits * 4);
@@ -373,21 +401,39 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       tc5::mbar_init(slot_full(i), 1);
-      tc5::mbar_init(slot_empty(i), HPC * WG);  // every warp of one chunk class
+      tc5::mbar_init(slot_empty(i), C::SLOT_EMPTY_N);  // every warp of one chunk class
     }
     for (int i = 0; i < C::NQ; ++i) {
       tc5::mbar_init(q_full(i), 1);
-      tc5::mbar_init(q_empty(i), C::NCW);
+      tc5::mbar_init(q_empty(i), C::Q_EMPTY_N);
+    }
+    if constexpr (C::TC) {
+      const int tcb = 2 * NSLOT + 2 * C::NQ;
+      for (int i = 0; i < 2; ++i) {
+        tc5::mbar_init(bar0 + 8u * (tcb + i), 1);      // s_full: MMA commit
+        tc5::mbar_init(bar0 + 8u * (tcb + 2 + i), C::SXW);  // s_free: softmax warps
+        tc5::mbar_init(bar0 + 8u * (tcb + 4 + i), C::SXW);  // p_full: softmax warps
+        tc5::mbar_init(bar0 + 8u * (tcb + 6 + i), 1);       // pv_done: MMA commit
+        tc5::mbar_init(bar0 + 8u * (tcb + 8 + i), C::SXW);  // q8_full: softmax warps
+      }
+      tc5::mbar_init(bar0 + 8u * (tcb + 10), 1);       // final drain
     }
     *abort_flag = 0;
     tc5::fence_mbar_init();
     tc5::prefetch_tmap(&kv_map);
+  }
+  if constexpr (C::TC) {
+    if (warp == C::SXW + 1) {  // 64 columns: S^T twice (16 each) and O^T (16)
+      tc5::tmem_alloc(sbase + C::TCS_OFF + (2 * 16 + 4 * 16 + 16) * 4, 64);
+      tc5::tmem_relinquish();
+    }
   }
   // Q slots start as zeros: a unit stages only its valid rows, and the rows
   // past them (masked, never written out) only need to be finite.
   for (int i = threadIdx.x; i < C::NQ * C::Q_BYTES / 16; i += C::THREADS)
     reinterpret_cast<uint4*>(smem + C::Q_OFF)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
+  if constexpr (C::TC) tc5::tc_fence_after();
 
   if (warp == 0) {
     // ------------------------------------------------ producer warp -----
@@ -583,6 +629,396 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         tc5::mbar_wait(slot_full(k % NSLOT), (k / NSLOT) & 1u, abort_flag, p.err, false);
     cp_async_wait<0>();
     __syncwarp();
+  } else if constexpr (C::TC) {
+    // ------------------------------ tensor-core form (fp8 cache) --------
+    // Warps 1..SXW (softmax warps): warp w covers keys 32 (w % 4) .. + 31 of
+    // every chunk -- TMEM lanes 32 (w % 4) .. + 31 of S^T, the lane quarter
+    // the warp may touch -- and half hf = (w - 1) / 4 of the work on them:
+    // query rows 8 hf .. 8 hf + 7 (S^T columns) and V columns 64 hf .. + 63.
+    // Per chunk a thread scales and masks its key's scores, turns them into
+    // f16 probabilities P^T in shared memory, and converts its key's V
+    // columns from E4M3 to f16.  At the end of a unit it owns V column
+    // 32 (w % 4) + lane of O^T for its 8 rows.  Warp SXW + 1 issues every
+    // MMA: S^T = K Q^T on the 8-bit path straight from the ring (Q split
+    // exactly into two E4M3 terms), then O^T += V^T P^T in f16.
+    constexpr int KCH = C::KPC;         // keys per chunk: the M of S^T
+    constexpr int SXW = C::SXW;
+    constexpr int NH = SXW / 4;         // halves of a key's work
+    constexpr int RPT = 16 / NH;        // query rows per thread
+    constexpr int VPT = C::DV / NH;     // V columns per thread
+    constexpr int NSX = 32 * SXW;       // softmax threads
+    constexpr int TCB = 2 * NSLOT + 2 * C::NQ;
+    auto s_full = [&](uint32_t i) { return bar0 + 8u * (TCB + i); };
+    auto s_free = [&](uint32_t i) { return bar0 + 8u * (TCB + 2 + i); };
+    auto p_full = [&](uint32_t i) { return bar0 + 8u * (TCB + 4 + i); };
+    auto pv_done = [&](uint32_t i) { return bar0 + 8u * (TCB + 6 + i); };
+    auto q8_full = [&](uint32_t i) { return bar0 + 8u * (TCB + 8 + i); };
+    const uint32_t fin_bar = bar0 + 8u * (TCB + 10);
+    float* qscale = reinterpret_cast<float*>(smem + C::TCS_OFF);  // [2][16]
+    float* red = qscale + 32;                                      // [4][16]
+    float* lsum = red + 64;                                        // [16]
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(lsum + 16);
+    const uint32_t v16 = sbase + C::V16_OFF;
+    auto pt_buf = [&](uint32_t i) { return sbase + C::PT_OFF + i * C::PT_BYTES; };
+    auto q8_buf = [&](uint32_t i) { return sbase + C::Q8_OFF + i * C::Q8_BYTES; };
+    constexpr uint32_t TM_O = 32;  // O^T columns; S^T buffers at 0 and 16
+    if (warp == SXW + 1) {
+      // ---------------------------------------------------- MMA warp ----
+      if (lane == 0) {
+        constexpr uint32_t ID_S = tc5::idesc_e4m3_f32(KCH, 16);
+        constexpr uint32_t ID_PV = tc5::idesc_f16_f32(C::DV, 16, /*a_mn=*/true, false);
+        uint32_t gc = 0, qc = 0;
+        bool ok = true;
+        for (;;) {
+          const uint32_t qslot = qc % C::NQ;
+          if (!tc5::mbar_wait(q_full(qslot), (qc / C::NQ) & 1u, abort_flag, p.err)) break;
+          const Unit un = *desc_of(qc % C::ND);
+          tc5::mbar_arrive(q_empty(qslot));
+          const uint32_t u = qc++;
+          if (un.nch < 0 || *abort_flag) break;
+          if (!tc5::mbar_wait(q8_full(u & 1u), (u >> 1) & 1u, abort_flag, p.err)) break;
+          const uint32_t qb = q8_buf(u & 1u);
+          for (int k = 0; k <= un.nch && ok; ++k) {
+            if (k < un.nch) {  // S^T(c) = K(c) Q^T, 6 k-steps of 32 x 2 Q terms
+              const uint32_t c = gc + k;
+              const uint32_t slot = c % NSLOT;
+              ok = tc5::mbar_wait(slot_full(slot), (c / NSLOT) & 1u, abort_flag, p.err) &&
+                   tc5::mbar_wait(s_free(c & 1u), ((c >> 1) & 1u) ^ 1u, abort_flag, p.err);
+              if (!ok) break;
+              tc5::tc_fence_after();
+              const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
+#pragma unroll
+              for (int ks = 0; ks < C::DK / 32; ++ks) {
+                const uint64_t ad =
+                    tc5::sdesc_sw128(st + (ks >> 2) * C::CB_STRIDE + (ks & 3) * 32, 16, 1024);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                  tc5::mma_f8f6f4_ss(
+                      tmem + 16u * (c & 1u), ad,
+                      tc5::sdesc_sw128(qb + t * (C::Q8_BYTES / 2) + (ks >> 2) * 2048 +
+                                           (ks & 3) * 32,
+                                       16, 1024),
+                      ID_S, (ks | t) ? 1u : 0u);
+              }
+              tc5::mma_commit(s_full(c & 1u));
+              tc5::mma_commit(slot_empty(slot));
+            }
+            if (k > 0) {  // O^T += V^T(c-1) P^T(c-1), 16 keys per MMA
+              const uint32_t c = gc + k - 1;
+              ok = tc5::mbar_wait(p_full(c & 1u), (c >> 1) & 1u, abort_flag, p.err);
+              if (!ok) break;
+              tc5::tc_fence_after();
+              const uint32_t pb = pt_buf(c & 1u);
+#pragma unroll
+              for (int kk = 0; kk < KCH / 16; ++kk)
+                tc5::mma_f16_ss(tmem + TM_O,
+                                tc5::sdesc_sw128(v16 + kk * 2048, KCH * 128, 1024),
+                                tc5::sdesc_sw128(pb + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
+                                ID_PV, (k > 1 || kk > 0) ? 1u : 0u);
+              tc5::mma_commit(pv_done(c & 1u));
+            }
+          }
+          if (!ok) break;
+          gc += un.nch;
+        }
+        // every MMA issued above has completed before TMEM is freed
+        tc5::mma_commit(fin_bar);
+        tc5::mbar_wait(fin_bar, 0, abort_flag, p.err, /*honor_abort=*/false);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------ softmax warps ----
+      constexpr float kTau = 8.f;  // P <= 2^8 between max updates (log2 units)
+      const int quad = warp & 3;
+      const int hf = (warp - 1) / 4;
+      const int r0 = RPT * hf;            // my first query row
+      const int kk = 32 * quad + lane;    // my key of a chunk / my column of O^T
+      const int sxid = threadIdx.x - 32;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+      const int vbyte0 = p.v_off - lo;    // V's first byte in the staged span
+      uint32_t gc = 0, qc = 0;
+      // reduce-scatter of RPT per-row values over the warp (max or sum): the
+      // lane ends with row r0 + (lane / (32 / RPT)) over the warp's 32 keys
+      auto warp_rows = [&](float (&v)[RPT], bool is_max) {
+#pragma unroll
+        for (int h = RPT / 2; h >= 1; h >>= 1) {
+          const int m = (32 / RPT) * h;  // partner lane distance; its bit picks the half kept
+          const bool up = (lane & m) != 0;
+#pragma unroll
+          for (int r = 0; r < h; ++r) {
+            const float send = up ? v[r] : v[r + h];
+            const float keep = up ? v[r + h] : v[r];
+            const float got = __shfl_xor_sync(0xffffffffu, send, m);
+            v[r] = is_max ? fmaxf(keep, got) : keep + got;
+          }
+        }
+#pragma unroll
+        for (int m = 16 / RPT; m >= 1; m >>= 1) {
+          const float got = __shfl_xor_sync(0xffffffffu, v[0], m);
+          v[0] = is_max ? fmaxf(v[0], got) : v[0] + got;
+        }
+        return v[0];
+      };
+      for (;;) {
+        const uint32_t qslot = qc % C::NQ;
+        tc5::mbar_wait(q_full(qslot), (qc / C::NQ) & 1u, abort_flag, p.err);
+        if (barrier_or(3, NSX, *abort_flag != 0)) break;
+        const Unit un = *desc_of(qc % C::ND);
+        if (un.nch < 0) break;
+        const uint32_t u = qc++;
+        const int kvh = un.hb;
+        if (sxid < 128) {
+          // ---- Q rows -> hi + lo E4M3 terms, scaled by 2^e per row so that
+          //      the row's largest |q| lands in [128, 256): for bf16 input the
+          //      two terms hold q exactly (hi keeps 4 significant bits, the
+          //      remainder has at most 4 more) wherever the remainder is
+          //      within E4M3's range ----
+          const uint32_t qsrc = sbase + C::Q_OFF + qslot * C::Q_BYTES;
+          const int r = sxid >> 3, g = sxid & 7;  // row, piece group of 3 x 8 columns
+          float x[24];
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const uint4 v = lds128(q_piece<C::DK>(qsrc, r, g + 8 * j));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[m]));
+              x[8 * j + 2 * m] = f.x;
+              x[8 * j + 2 * m + 1] = f.y;
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+          int e = 0;
+          if (amax > 0.f)
+            e = min(7 - (static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127), 126);
+          const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);  // 2^e
+          if (g == 0) qscale[(u & 1u) * 16 + r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+          const uint32_t qb = q8_buf(u & 1u);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            uint32_t hi[2], lo8[2];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float a = x[8 * j + 2 * m] * sc, b = x[8 * j + 2 * m + 1] * sc;
+              const uint16_t h = static_cast<uint16_t>(
+                  __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+              const uint32_t hf2 = e4m3x2_to_f16x2(h);
+              const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hf2));
+              const uint16_t l = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+                  make_float2(a - hv.x, b - hv.y), __NV_SATFINITE, __NV_E4M3));
+              if (m & 1) {
+                hi[m >> 1] |= static_cast<uint32_t>(h) << 16;
+                lo8[m >> 1] |= static_cast<uint32_t>(l) << 16;
+              } else {
+                hi[m >> 1] = h;
+                lo8[m >> 1] = l;
+              }
+            }
+            const int d0 = 8 * (g + 8 * j);  // first of this piece's 8 columns
+            const uint32_t off = (d0 >> 7) * 2048 + r * 128 +
+                                 ((((d0 & 127) >> 4) ^ (r & 7)) << 4) + (d0 & 15);
+            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qb + off), "r"(hi[0]),
+                         "r"(hi[1]) : "memory");
+            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qb + C::Q8_BYTES / 2 + off),
+                         "r"(lo8[0]), "r"(lo8[1]) : "memory");
+          }
+          tc5::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc5::mbar_arrive(q8_full(u & 1u));
+          tc5::mbar_arrive(q_empty(qslot));
+        }
+        named_barrier(3, NSX);  // the row scales are visible
+        const int sidx = p.scale_mode == PKV_SCALE_HEAD ? kvh : 0;
+        const float base_scale = p.softmax_scale * kLog2e * __ldg(p.k_scale + sidx);
+        float qs[RPT], m_ref[RPT], l[RPT];
+        int vis[RPT];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+          const int r = r0 + j;
+          qs[j] = base_scale * qscale[(u & 1u) * 16 + r];
+          m_ref[j] = -INFINITY;
+          l[j] = 0.f;
+          vis[j] = 0;
+          if (r < un.nrows) {
+            const int i = (un.row0 + r) / G;
+            vis[j] = min(un.khi, max(0, min(un.L, un.L - un.qlen + i + 1)));
+          }
+        }
+        for (int k = 0; k < un.nch; ++k) {
+          const uint32_t c = gc + k;
+          const uint32_t slot = c % NSLOT;
+          const int key = un.klo + k * KCH + kk;
+          // ---- my key's scores for my rows (log2 domain), masked ----
+          tc5::mbar_wait(s_full(c & 1u), (c >> 1) & 1u, abort_flag, p.err);
+          tc5::tc_fence_after();
+          uint32_t sr[RPT];
+          tc5::tmem_ld_32x32b_x8(tl + 16u * (c & 1u) + r0, sr);
+          tc5::tmem_wait_ld();
+          tc5::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc5::mbar_arrive(s_free(c & 1u));
+          float x[RPT];
+          bool need = false;
+#pragma unroll
+          for (int j = 0; j < RPT; ++j) {
+            x[j] = key < vis[j] ? __uint_as_float(sr[j]) * qs[j] : -INFINITY;
+            need |= x[j] > m_ref[j] + kTau;
+          }
+          if (barrier_or(3, NSX, need)) {
+            // a score passed its row's reference by more than kTau: take the
+            // chunk's exact row maxima, move the references up and rescale
+            // what was accumulated (O^T in TMEM, this thread's row sums)
+            float v[RPT];
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) v[j] = x[j];
+            const float wm = warp_rows(v, true);
+            if ((lane & (32 / RPT - 1)) == 0) red[quad * 16 + r0 + lane / (32 / RPT)] = wm;
+            named_barrier(3, NSX);
+            float alpha[RPT];
+            bool rescale = false;
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+              const int r = r0 + j;
+              const float cm = fmaxf(fmaxf(red[r], red[16 + r]), fmaxf(red[32 + r], red[48 + r]));
+              const float mn = fmaxf(m_ref[j], cm);
+              alpha[j] = m_ref[j] == -INFINITY ? 1.f : fast_exp2(m_ref[j] - mn);
+              rescale |= alpha[j] != 1.f;
+              m_ref[j] = mn;
+              l[j] *= alpha[j];
+            }
+            named_barrier(3, NSX);  // red[] is read before it is written again
+            if (k > 0 && rescale) {
+              const uint32_t cp = c - 1;
+              tc5::mbar_wait(pv_done(cp & 1u), (cp >> 1) & 1u, abort_flag, p.err);
+              tc5::tc_fence_after();
+              uint32_t o[RPT];
+              tc5::tmem_ld_32x32b_x8(tl + TM_O + r0, o);
+              tc5::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < RPT; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
+              tc5::tmem_st_32x32b_x8(tl + TM_O + r0, o);
+              tc5::tmem_wait_st();
+              tc5::tc_fence_before();
+            }
+          }
+          float pr[RPT];
+#pragma unroll
+          for (int j = 0; j < RPT; ++j) {
+            pr[j] = fast_exp2(x[j] - (m_ref[j] == -INFINITY ? 0.f : m_ref[j]));
+            l[j] += pr[j];
+          }
+          // ---- P^T (f16) for the B operand: [64-key atom][16 rows][128 B];
+          //      lane pairs swap values so each store holds two keys ----
+          if (c >= 2) tc5::mbar_wait(pv_done(c & 1u), ((c - 2) >> 1) & 1u, abort_flag, p.err);
+          {
+            const uint32_t pb = pt_buf(c & 1u);
+            const int k0 = kk & ~1;
+            const bool odd = lane & 1;
+            const uint32_t pbase = pb + (k0 >> 6) * 2048 + (k0 & 7) * 2;
+            const int kc = (k0 & 63) >> 3;
+#pragma unroll
+            for (int j = 0; j < RPT / 2; ++j) {
+              const float send = odd ? pr[2 * j] : pr[2 * j + 1];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+              const int r = r0 + 2 * j + (odd ? 1 : 0);
+              const uint32_t val = odd ? pack_f16x2(recv, pr[2 * j + 1]) : pack_f16x2(pr[2 * j], recv);
+              asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(pbase + r * 128 + ((kc ^ (r & 7)) << 4)),
+                           "r"(val) : "memory");
+            }
+          }
+          // ---- my key's V columns, E4M3 -> f16, into [64-column slab][key]
+          //      [128 B] (zeros past the last key any row sees) ----
+          tc5::mbar_wait(slot_full(slot), (c / NSLOT) & 1u, abort_flag, p.err);
+          if (c >= 1) tc5::mbar_wait(pv_done((c - 1) & 1u), ((c - 1) >> 1) & 1u, abort_flag, p.err);
+          {
+            const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
+            const bool valid = key < un.kmax;
+#pragma unroll
+            for (int i = 0; i < VPT / 16; ++i) {
+              const int d0 = VPT * hf + 16 * i;  // first of these 16 V columns
+              const int byte = vbyte0 + d0;
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (valid)
+                w = lds128(st + (byte >> 7) * C::CB_STRIDE + kk * 128 +
+                           ((((byte & 127) >> 4) ^ (kk & 7)) << 4));
+              const uint32_t h[8] = {
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16))};
+              const uint32_t srow = v16 + (d0 >> 6) * (KCH * 128) + kk * 128;
+              const int pc0 = (d0 & 63) >> 3;
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + ((pc0 ^ (kk & 7)) << 4)),
+                           "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((pc0 + 1) ^ (kk & 7)) << 4)),
+                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+            }
+          }
+          tc5::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc5::mbar_arrive(p_full(c & 1u));
+            tc5::mbar_arrive(slot_empty(slot));
+          }
+        }
+        gc += un.nch;
+        // ---- row sums over all keys of the unit, then the partials ----
+        {
+          float v[RPT];
+#pragma unroll
+          for (int j = 0; j < RPT; ++j) v[j] = l[j];
+          const float ws = warp_rows(v, false);
+          if ((lane & (32 / RPT - 1)) == 0) red[quad * 16 + r0 + lane / (32 / RPT)] = ws;
+        }
+        named_barrier(3, NSX);
+        if (sxid < 16) lsum[sxid] = red[sxid] + red[16 + sxid] + red[32 + sxid] + red[48 + sxid];
+        named_barrier(3, NSX);
+        float L[RPT];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) L[j] = lsum[r0 + j];
+        auto orow_of = [&](int r) {
+          const int rr = un.row0 + r;
+          const int64_t t = un.qs + rr / G;
+          return (un.s * T + t) * p.num_q_heads + kvh * G + rr % G;
+        };
+        if (un.nch > 0) {
+          const uint32_t cl = gc - 1;
+          tc5::mbar_wait(pv_done(cl & 1u), (cl >> 1) & 1u, abort_flag, p.err);
+          tc5::tc_fence_after();
+          uint32_t o[RPT];
+          tc5::tmem_ld_32x32b_x8(tl + TM_O + r0, o);
+          tc5::tmem_wait_ld();
+          tc5::tc_fence_before();
+          const float vm = __ldg(p.v_scale + sidx);
+#pragma unroll
+          for (int j = 0; j < RPT; ++j)
+            if (r0 + j < un.nrows && L[j] > 0.f)
+              p.partial_o[orow_of(r0 + j) * C::DV + kk] = __uint_as_float(o[j]) * (vm / L[j]);
+        }
+        // the lse of row r: the thread of the first softmax warp's half
+        // that holds it (lane r - r0), from its own row references
+        if (quad == 1 && lane < RPT && r0 + lane < un.nrows) {
+          float mr = 0.f, lr = 0.f;
+#pragma unroll
+          for (int j = 0; j < RPT; ++j)
+            if (j == lane) {
+              mr = m_ref[j];
+              lr = L[j];
+            }
+          p.partial_lse[orow_of(r0 + lane)] = lr > 0.f ? (mr + fast_log2(lr)) * kLn2 : -INFINITY;
+        }
+        if (p.fused) fused_finish<C>(p, un, us.HB, us.RG, smem, sxid);
+      }
+    }
+    // TMEM is freed once the MMAs have drained and no warp reads it
+    named_barrier(4, 32 * (SXW + 1));
+    if (warp == SXW + 1) tc5::tmem_dealloc(tmem, 64);
   } else if constexpr (C::NARROW) {
     // --------------------------------------- consumer warps, narrow form --
     // A head's rows fit in 8 (q_len * G <= 8): S^T = K Q^T with the 16 keys
@@ -1234,6 +1670,9 @@ using CfgBf16_192x1 = DecodeCfg<192, 128, false, 1, 1, 6, 16, 12, 4, 320>;
 // K192 / V128, fp8: one head, 64 keys per chunk (three 8 KB boxes at block
 // 64), six chunk classes.
 using CfgFp8_192 = DecodeCfg<192, 128, true, 1, 1, 6, 64, 6, 2, 320>;
+// The same on the tensor cores: one head, 128 keys per chunk (40 KB),
+// three ring slots; for rows whose K precedes V.
+using CfgFp8_192tc = DecodeCfg<192, 128, true, 1, 1, 1, 128, 3, 2, 320, false, 1, true>;
 // MLA 576 / 512: one latent head, 32 (bf16) or 64 (fp8) keys per chunk.
 using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 2, 1, 576, false, 2>;
 using CfgFp8_576 = DecodeCfg<576, 512, true, 1, 4, 1, 64, 4, 2, 576>;
@@ -1249,7 +1688,9 @@ bool decode_supported(int head_size, int head_size_v, int dtype) {
 cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream) {
   const bool fp8 = p.dtype == PKV_FP8_E4M3;
   if (p.head_size == 192 && p.head_size_v == 128) {
-    if (fp8) return launch_cfg<CfgFp8_192>(p, num_sms, stream);
+    if (fp8)
+      return p.k_off <= p.v_off ? launch_cfg<CfgFp8_192tc>(p, num_sms, stream)
+                                : launch_cfg<CfgFp8_192>(p, num_sms, stream);
     if (p.num_kv_heads % 4 != 0) return launch_cfg<CfgBf16_192x1>(p, num_sms, stream);
     return p.max_query_len * p.group <= 8 ? launch_cfg<CfgBf16_192x4n>(p, num_sms, stream)
                                           : launch_cfg<CfgBf16_192x4>(p, num_sms, stream);
