@@ -85,7 +85,11 @@ struct DecodeCfg {
   // slice are adjacent (CB_STRIDE) so that one TMA box can bring them all.
   static constexpr int CB_BYTES = KPC * 128;
   static constexpr int CB_STRIDE = HPC * CB_BYTES;
-  static constexpr int SLOT_BYTES = NBOX * CB_STRIDE;
+  // tensor-core form: the third column box is 64 bytes wide (span bytes
+  // 256..319, 64-byte swizzle), so a slot holds no padding
+  static constexpr int SLOT_BYTES = TC ? 2 * CB_STRIDE + KPC * 64 : NBOX * CB_STRIDE;
+  // bytes a chunk's boxes bring per key row of one head
+  static constexpr int ROW_BYTES = TC ? 320 : NBOX * 128;
   static constexpr int NGRP = HPC * NG;                  // consumer groups
   static constexpr int SXW = TC ? 8 : 0;                 // softmax warps (TC)
   static constexpr int NCW = TC ? SXW + 1 : NGRP * WG;   // consumer warps
@@ -108,15 +112,16 @@ struct DecodeCfg {
   static constexpr int DVP = DV + 4;
   static constexpr int RING_OFF = 0;
   // tensor-core form: V converted to f16 ([64-column slab][KPC keys][128 B],
-  // 128-byte swizzle), P^T in f16 ([64-key atom][16 rows][128 B]) twice, and
-  // Q as two E4M3 terms ([term][128-column atom][16 rows][128 B]) twice
+  // 128-byte swizzle) twice, P^T in f16 ([64-key atom][16 rows][128 B])
+  // twice, and Q as two E4M3 terms stacked as 32 rows ([128-column atom][hi
+  // rows 0..15, lo rows 16..31][128 B]) once
   static constexpr int V16_OFF = RING_OFF + NSLOT * SLOT_BYTES;
   static constexpr int V16_BYTES = TC ? (DV / 64) * KPC * 128 : 0;
-  static constexpr int PT_OFF = V16_OFF + V16_BYTES;
+  static constexpr int PT_OFF = V16_OFF + 2 * V16_BYTES;
   static constexpr int PT_BYTES = TC ? (KPC / 64) * 16 * 128 : 0;
   static constexpr int Q8_OFF = PT_OFF + 2 * PT_BYTES;
-  static constexpr int Q8_BYTES = TC ? 2 * ((DK + 127) / 128) * 16 * 128 : 0;
-  static constexpr int Q_OFF = Q8_OFF + 2 * Q8_BYTES;
+  static constexpr int Q8_BYTES = TC ? ((DK + 127) / 128) * 32 * 128 : 0;
+  static constexpr int Q_OFF = Q8_OFF + Q8_BYTES;
   static constexpr int DESC_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int DESC_BYTES = 64 + MAXP * 4;  // descriptor + page ids
   // Descriptor slots: two at least, so that staging unit n+1 (while unit n
@@ -366,7 +371,8 @@ __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS)
-    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p,
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map,
+                  const __grid_constant__ CUtensorMap kv_map64, const AttnParams p,
                   int head_boxes) {
   extern __shared__ uint8_t smem_raw[];
   constexpr bool FP8 = C::FP8;
@@ -421,10 +427,11 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     *abort_flag = 0;
     tc5::fence_mbar_init();
     tc5::prefetch_tmap(&kv_map);
+    if constexpr (C::TC) tc5::prefetch_tmap(&kv_map64);
   }
   if constexpr (C::TC) {
-    if (warp == C::SXW + 1) {  // 64 columns: S^T twice (16 each) and O^T (16)
-      tc5::tmem_alloc(sbase + C::TCS_OFF + (2 * 16 + 4 * 16 + 16) * 4, 64);
+    if (warp == C::SXW + 1) {  // 128 columns: S^T twice (32 each) and O^T (16)
+      tc5::tmem_alloc(sbase + C::TCS_OFF + (2 * 16 + 4 * 16 + 16) * 4, 128);
       tc5::tmem_relinquish();
     }
   }
@@ -578,7 +585,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         const int per_head = C::NBOX * nvr;
         if (lane == 0)
           tc5::mbar_arrive_expect_tx(slot_full(slot),
-                                     static_cast<uint32_t>(HPC * per_head * box_rows * 128));
+                                     static_cast<uint32_t>(HPC * nvr * box_rows * C::ROW_BYTES));
         __syncwarp();
         const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
         const int nboxes = head_boxes ? C::NBOX : HPC * per_head;
@@ -593,10 +600,16 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
             set_dev_error(p.err, PKV_EDEV_RANGE);
             page = p.num_blocks;  // out-of-range box: TMA fills zeros
           }
-          const uint32_t dst = st + cb * C::CB_STRIDE + h * C::CB_BYTES + rb * box_rows * 128;
+          const uint32_t dst = st + cb * C::CB_STRIDE + h * C::CB_BYTES +
+                               rb * box_rows * (C::TC && cb == 2 ? 64 : 128);
           const int col = lo + cb * C::BOX_COLS;
           const int head = un.hb * HPC + h;
-          if (head_boxes)  // (col, slot, head, page) in both layouts
+          if (C::TC && cb == 2) {  // the 64-byte third box
+            if (p.layout == PKV_NHD)
+              tc5::tma_load_4d(dst, &kv_map64, col, head, key0 % bs, page, slot_full(slot));
+            else
+              tc5::tma_load_4d(dst, &kv_map64, col, key0 % bs, head, page, slot_full(slot));
+          } else if (head_boxes)  // (col, slot, head, page) in both layouts
             tc5::tma_load_4d(dst, &kv_map, col, key0 % bs, head, page, slot_full(slot));
           else if (p.layout == PKV_NHD)
             tc5::tma_load_4d(dst, &kv_map, col, head, key0 % bs, page, slot_full(slot));
@@ -640,7 +653,8 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     // columns from E4M3 to f16.  At the end of a unit it owns V column
     // 32 (w % 4) + lane of O^T for its 8 rows.  Warp SXW + 1 issues every
     // MMA: S^T = K Q^T on the 8-bit path straight from the ring (Q split
-    // exactly into two E4M3 terms), then O^T += V^T P^T in f16.
+    // exactly into two E4M3 terms, stacked as N = 32: S^T columns 0..15 are
+    // the hi products, 16..31 the lo ones), then O^T += V^T P^T in f16.
     constexpr int KCH = C::KPC;         // keys per chunk: the M of S^T
     constexpr int SXW = C::SXW;
     constexpr int NH = SXW / 4;         // halves of a key's work
@@ -658,14 +672,14 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     float* red = qscale + 32;                                      // [4][16]
     float* lsum = red + 64;                                        // [16]
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(lsum + 16);
-    const uint32_t v16 = sbase + C::V16_OFF;
+    auto v16_buf = [&](uint32_t i) { return sbase + C::V16_OFF + i * C::V16_BYTES; };
     auto pt_buf = [&](uint32_t i) { return sbase + C::PT_OFF + i * C::PT_BYTES; };
-    auto q8_buf = [&](uint32_t i) { return sbase + C::Q8_OFF + i * C::Q8_BYTES; };
-    constexpr uint32_t TM_O = 32;  // O^T columns; S^T buffers at 0 and 16
+    const uint32_t q8 = sbase + C::Q8_OFF;
+    constexpr uint32_t TM_O = 64;  // O^T columns; S^T buffers (32 wide) at 0 and 32
     if (warp == SXW + 1) {
       // ---------------------------------------------------- MMA warp ----
       if (lane == 0) {
-        constexpr uint32_t ID_S = tc5::idesc_e4m3_f32(KCH, 16);
+        constexpr uint32_t ID_S = tc5::idesc_e4m3_f32(KCH, 32);
         constexpr uint32_t ID_PV = tc5::idesc_f16_f32(C::DV, 16, /*a_mn=*/true, false);
         uint32_t gc = 0, qc = 0;
         bool ok = true;
@@ -676,10 +690,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           tc5::mbar_arrive(q_empty(qslot));
           const uint32_t u = qc++;
           if (un.nch < 0 || *abort_flag) break;
-          if (!tc5::mbar_wait(q8_full(u & 1u), (u >> 1) & 1u, abort_flag, p.err)) break;
-          const uint32_t qb = q8_buf(u & 1u);
+          if (!tc5::mbar_wait(q8_full(0), u & 1u, abort_flag, p.err)) break;
+          const uint32_t qb = q8;
           for (int k = 0; k <= un.nch && ok; ++k) {
-            if (k < un.nch) {  // S^T(c) = K(c) Q^T, 6 k-steps of 32 x 2 Q terms
+            if (k < un.nch) {  // S^T(c) = K(c) [Q_hi; Q_lo]^T, 6 k-steps of 32
               const uint32_t c = gc + k;
               const uint32_t slot = c % NSLOT;
               ok = tc5::mbar_wait(slot_full(slot), (c / NSLOT) & 1u, abort_flag, p.err) &&
@@ -688,18 +702,12 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
               tc5::tc_fence_after();
               const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
 #pragma unroll
-              for (int ks = 0; ks < C::DK / 32; ++ks) {
-                const uint64_t ad =
-                    tc5::sdesc_sw128(st + (ks >> 2) * C::CB_STRIDE + (ks & 3) * 32, 16, 1024);
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-                  tc5::mma_f8f6f4_ss(
-                      tmem + 16u * (c & 1u), ad,
-                      tc5::sdesc_sw128(qb + t * (C::Q8_BYTES / 2) + (ks >> 2) * 2048 +
-                                           (ks & 3) * 32,
-                                       16, 1024),
-                      ID_S, (ks | t) ? 1u : 0u);
-              }
+              for (int ks = 0; ks < C::DK / 32; ++ks)
+                tc5::mma_f8f6f4_ss(
+                    tmem + 32u * (c & 1u),
+                    tc5::sdesc_sw128(st + (ks >> 2) * C::CB_STRIDE + (ks & 3) * 32, 16, 1024),
+                    tc5::sdesc_sw128(qb + (ks >> 2) * 4096 + (ks & 3) * 32, 16, 1024), ID_S,
+                    ks ? 1u : 0u);
               tc5::mma_commit(s_full(c & 1u));
               tc5::mma_commit(slot_empty(slot));
             }
@@ -709,10 +717,11 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
               if (!ok) break;
               tc5::tc_fence_after();
               const uint32_t pb = pt_buf(c & 1u);
+              const uint32_t vb = v16_buf(c & 1u);
 #pragma unroll
               for (int kk = 0; kk < KCH / 16; ++kk)
                 tc5::mma_f16_ss(tmem + TM_O,
-                                tc5::sdesc_sw128(v16 + kk * 2048, KCH * 128, 1024),
+                                tc5::sdesc_sw128(vb + kk * 2048, KCH * 128, 1024),
                                 tc5::sdesc_sw128(pb + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
                                 ID_PV, (k > 1 || kk > 0) ? 1u : 0u);
               tc5::mma_commit(pv_done(c & 1u));
@@ -797,7 +806,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
             e = min(7 - (static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127), 126);
           const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);  // 2^e
           if (g == 0) qscale[(u & 1u) * 16 + r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-          const uint32_t qb = q8_buf(u & 1u);
+          // one Q buffer: every S^T MMA of the previous unit has completed,
+          // since this thread has read all of their results
+          const uint32_t qb = q8;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             uint32_t hi[2], lo8[2];
@@ -819,18 +830,18 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
               }
             }
             const int d0 = 8 * (g + 8 * j);  // first of this piece's 8 columns
-            const uint32_t off = (d0 >> 7) * 2048 + r * 128 +
+            const uint32_t off = (d0 >> 7) * 4096 + r * 128 +
                                  ((((d0 & 127) >> 4) ^ (r & 7)) << 4) + (d0 & 15);
             asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qb + off), "r"(hi[0]),
                          "r"(hi[1]) : "memory");
-            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qb + C::Q8_BYTES / 2 + off),
+            asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(qb + 16 * 128 + off),
                          "r"(lo8[0]), "r"(lo8[1]) : "memory");
           }
           tc5::fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) {
-          tc5::mbar_arrive(q8_full(u & 1u));
+          tc5::mbar_arrive(q8_full(0));
           tc5::mbar_arrive(q_empty(qslot));
         }
         named_barrier(3, NSX);  // the row scales are visible
@@ -854,11 +865,53 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           const uint32_t c = gc + k;
           const uint32_t slot = c % NSLOT;
           const int key = un.klo + k * KCH + kk;
+          // ---- my key's V columns, E4M3 -> f16, into [64-column slab][key]
+          //      [128 B] of buffer c % 2 (zeros past the last key any row
+          //      sees); its previous user PV(c - 2) has completed, and so has
+          //      the P^T buffer's.  The ring slot is released right after. ----
+          tc5::mbar_wait(slot_full(slot), (c / NSLOT) & 1u, abort_flag, p.err);
+          if (c >= 2) tc5::mbar_wait(pv_done(c & 1u), ((c - 2) >> 1) & 1u, abort_flag, p.err);
+          {
+            const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
+            const uint32_t vb = v16_buf(c & 1u);
+            const bool valid = key < un.kmax;
+#pragma unroll
+            for (int i = 0; i < VPT / 16; ++i) {
+              const int d0 = VPT * hf + 16 * i;  // first of these 16 V columns
+              const int byte = vbyte0 + d0;
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (valid) {
+                uint32_t a;
+                if (byte < 256) {  // 128-byte rows, 128-byte swizzle
+                  a = st + (byte >> 7) * C::CB_STRIDE + kk * 128 +
+                      ((((byte & 127) >> 4) ^ (kk & 7)) << 4);
+                } else {  // the third box: 64-byte rows, 64-byte swizzle
+                  const uint32_t o = kk * 64 + (byte - 256);
+                  a = st + 2 * C::CB_STRIDE + (o ^ (((o >> 7) & 3u) << 4));
+                }
+                w = lds128(a);
+              }
+              const uint32_t h[8] = {
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16))};
+              const uint32_t srow = vb + (d0 >> 6) * (KCH * 128) + kk * 128;
+              const int pc0 = (d0 & 63) >> 3;
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + ((pc0 ^ (kk & 7)) << 4)),
+                           "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((pc0 + 1) ^ (kk & 7)) << 4)),
+                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+            }
+          }
+          __syncwarp();
+          if (lane == 0) tc5::mbar_arrive(slot_empty(slot));
           // ---- my key's scores for my rows (log2 domain), masked ----
           tc5::mbar_wait(s_full(c & 1u), (c >> 1) & 1u, abort_flag, p.err);
           tc5::tc_fence_after();
-          uint32_t sr[RPT];
-          tc5::tmem_ld_32x32b_x8(tl + 16u * (c & 1u) + r0, sr);
+          uint32_t sr[RPT], sl[RPT];
+          tc5::tmem_ld_32x32b_x8(tl + 32u * (c & 1u) + r0, sr);
+          tc5::tmem_ld_32x32b_x8(tl + 32u * (c & 1u) + 16 + r0, sl);
           tc5::tmem_wait_ld();
           tc5::tc_fence_before();
           __syncwarp();
@@ -867,7 +920,8 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           bool need = false;
 #pragma unroll
           for (int j = 0; j < RPT; ++j) {
-            x[j] = key < vis[j] ? __uint_as_float(sr[j]) * qs[j] : -INFINITY;
+            x[j] = key < vis[j] ? (__uint_as_float(sr[j]) + __uint_as_float(sl[j])) * qs[j]
+                                : -INFINITY;
             need |= x[j] > m_ref[j] + kTau;
           }
           if (barrier_or(3, NSX, need)) {
@@ -915,7 +969,6 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           }
           // ---- P^T (f16) for the B operand: [64-key atom][16 rows][128 B];
           //      lane pairs swap values so each store holds two keys ----
-          if (c >= 2) tc5::mbar_wait(pv_done(c & 1u), ((c - 2) >> 1) & 1u, abort_flag, p.err);
           {
             const uint32_t pb = pt_buf(c & 1u);
             const int k0 = kk & ~1;
@@ -932,40 +985,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
                            "r"(val) : "memory");
             }
           }
-          // ---- my key's V columns, E4M3 -> f16, into [64-column slab][key]
-          //      [128 B] (zeros past the last key any row sees) ----
-          tc5::mbar_wait(slot_full(slot), (c / NSLOT) & 1u, abort_flag, p.err);
-          if (c >= 1) tc5::mbar_wait(pv_done((c - 1) & 1u), ((c - 1) >> 1) & 1u, abort_flag, p.err);
-          {
-            const uint32_t st = sbase + C::RING_OFF + slot * C::SLOT_BYTES;
-            const bool valid = key < un.kmax;
-#pragma unroll
-            for (int i = 0; i < VPT / 16; ++i) {
-              const int d0 = VPT * hf + 16 * i;  // first of these 16 V columns
-              const int byte = vbyte0 + d0;
-              uint4 w = make_uint4(0, 0, 0, 0);
-              if (valid)
-                w = lds128(st + (byte >> 7) * C::CB_STRIDE + kk * 128 +
-                           ((((byte & 127) >> 4) ^ (kk & 7)) << 4));
-              const uint32_t h[8] = {
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)), e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16))};
-              const uint32_t srow = v16 + (d0 >> 6) * (KCH * 128) + kk * 128;
-              const int pc0 = (d0 & 63) >> 3;
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + ((pc0 ^ (kk & 7)) << 4)),
-                           "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((pc0 + 1) ^ (kk & 7)) << 4)),
-                           "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
-            }
-          }
-          tc5::fence_proxy_async_smem();
+          tc5::fence_proxy_async_smem();  // V and P^T -> the tensor core
           __syncwarp();
-          if (lane == 0) {
-            tc5::mbar_arrive(p_full(c & 1u));
-            tc5::mbar_arrive(slot_empty(slot));
-          }
+          if (lane == 0) tc5::mbar_arrive(p_full(c & 1u));
         }
         gc += un.nch;
         // ---- row sums over all keys of the unit, then the partials ----
@@ -1018,7 +1040,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     }
     // TMEM is freed once the MMAs have drained and no warp reads it
     named_barrier(4, 32 * (SXW + 1));
-    if (warp == SXW + 1) tc5::tmem_dealloc(tmem, 64);
+    if (warp == SXW + 1) tc5::tmem_dealloc(tmem, 128);
   } else if constexpr (C::NARROW) {
     // --------------------------------------- consumer warps, narrow form --
     // A head's rows fit in 8 (q_len * G <= 8): S^T = K Q^T with the 16 keys
@@ -1650,12 +1672,19 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                    p.block_size, p.num_kv_heads, p.row_elems, C::BOX_COLS,
                                    box_rows);
   if (!ok) return cudaErrorInvalidValue;
+  // tensor-core form: the third column box (span bytes 256..319) is 64 bytes
+  // wide with a 64-byte swizzle
+  alignas(64) CUtensorMap kv_map64 = kv_map;
+  if (C::TC && !make_cache_tmap(&kv_map64, p.cache, p.dtype, p.layout, p.num_blocks,
+                                p.block_size, p.num_kv_heads, p.row_elems, 64, box_rows,
+                                /*swizzle64=*/true))
+    return cudaErrorInvalidValue;
   const int64_t RG = (static_cast<int64_t>(p.max_query_len) * p.group + 15) / 16;
   const int64_t units = static_cast<int64_t>(p.num_splits) * p.num_seqs *
                         (p.num_kv_heads / C::HPC) * RG;
   const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
   const int grid = static_cast<int>(units < slots ? units : slots);
-  decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, p, head_boxes);
+  decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, kv_map64, p, head_boxes);
   return cudaGetLastError();
 }
 

@@ -27,14 +27,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
   return fn;
 }
 
-// A 4-D map over the cache whose boxes are `box_cols` row elements wide (one
-// 128-byte swizzle span) and `box_rows` token slots high, for one KV head of
-// one page.  Coordinates: NHD (col, head, slot, page), HND (col, slot, head,
-// page).  Columns past row_elems read as zero.
+// A 4-D map over the cache whose boxes are `box_cols` row elements wide (at
+// most one swizzle span: 128 bytes, or 64 with swizzle64) and `box_rows`
+// token slots high, for one KV head of one page.  Coordinates: NHD (col,
+// head, slot, page), HND (col, slot, head, page).  Columns past row_elems
+// read as zero.
 inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
                             int layout, int num_blocks, int block_size,
                             int num_kv_heads, int row_elems, int box_cols,
-                            int box_rows) {
+                            int box_rows, bool swizzle64 = false) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encode_fn();
   if (encode == nullptr) return false;
   const cuuint64_t e = dtype == PKV_FP8_E4M3 ? 1 : 2;
@@ -57,7 +58,8 @@ inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
                 dtype == PKV_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                 4, const_cast<void*>(cache), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
