@@ -145,8 +145,9 @@ struct DecodeCfg {
   static constexpr int BAR_OFF = (SBUF >= WBUF || MERGE >= WBUF) ? SBUF_OFF + SBUF
                                                                  : SBUF_OFF + SBUF + WBUF;
   // tensor-core form: s_full[2], s_free[2], p_full[2], pv_done[2],
-  // q8_full[2], final; then scratch: per-row Q scales [2][16], the row
-  // reductions [4 warps][16], the row sums [16] and the TMEM address
+  // q8_full (+1 spare), and the MMA warp's drain barrier; then scratch:
+  // per-row Q scales [2][16], the row reductions [4 warps][16], the row
+  // sums [16] and the TMEM address
   static constexpr int NBAR_TC = TC ? 11 : 0;
   static constexpr int NBAR = 2 * NSLOT + 2 * NQ + NBAR_TC;
   static constexpr int TCS_OFF = BAR_OFF + NBAR * 8 + 16;
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         tc5::mbar_init(bar0 + 8u * (tcb + 6 + i), 1);       // pv_done: MMA commit
         tc5::mbar_init(bar0 + 8u * (tcb + 8 + i), C::SXW);  // q8_full: softmax warps
       }
-      tc5::mbar_init(bar0 + 8u * (tcb + 10), 1);       // final drain
+      tc5::mbar_init(bar0 + 8u * (tcb + 10), 1);       // the MMA warp's drain
     }
     *abort_flag = 0;
     tc5::fence_mbar_init();
@@ -654,7 +655,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     // 32 (w % 4) + lane of O^T for its 8 rows.  Warp SXW + 1 issues every
     // MMA: S^T = K Q^T on the 8-bit path straight from the ring (Q split
     // exactly into two E4M3 terms, stacked as N = 32: S^T columns 0..15 are
-    // the hi products, 16..31 the lo ones), then O^T += V^T P^T in f16.
+    // the hi products, 16..31 the lo ones), and O^T += V^T P^T in f16.
     constexpr int KCH = C::KPC;         // keys per chunk: the M of S^T
     constexpr int SXW = C::SXW;
     constexpr int NH = SXW / 4;         // halves of a key's work
@@ -691,7 +692,6 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           const uint32_t u = qc++;
           if (un.nch < 0 || *abort_flag) break;
           if (!tc5::mbar_wait(q8_full(0), u & 1u, abort_flag, p.err)) break;
-          const uint32_t qb = q8;
           for (int k = 0; k <= un.nch && ok; ++k) {
             if (k < un.nch) {  // S^T(c) = K(c) [Q_hi; Q_lo]^T, 6 k-steps of 32
               const uint32_t c = gc + k;
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
                 tc5::mma_f8f6f4_ss(
                     tmem + 32u * (c & 1u),
                     tc5::sdesc_sw128(st + (ks >> 2) * C::CB_STRIDE + (ks & 3) * 32, 16, 1024),
-                    tc5::sdesc_sw128(qb + (ks >> 2) * 4096 + (ks & 3) * 32, 16, 1024), ID_S,
+                    tc5::sdesc_sw128(q8 + (ks >> 2) * 4096 + (ks & 3) * 32, 16, 1024), ID_S,
                     ks ? 1u : 0u);
               tc5::mma_commit(s_full(c & 1u));
               tc5::mma_commit(slot_empty(slot));
@@ -768,14 +768,17 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         }
         return v[0];
       };
-      for (;;) {
+      // The next staged unit: its descriptor, and its Q rows split into the
+      // Q buffer with their scales (every S^T MMA of the previous unit has
+      // completed: this thread has read all of their results).  False at the
+      // end marker or after a timeout, the same in all softmax threads.
+      auto fetch = [&](Unit& un, uint32_t& u) -> bool {
         const uint32_t qslot = qc % C::NQ;
         tc5::mbar_wait(q_full(qslot), (qc / C::NQ) & 1u, abort_flag, p.err);
-        if (barrier_or(3, NSX, *abort_flag != 0)) break;
-        const Unit un = *desc_of(qc % C::ND);
-        if (un.nch < 0) break;
-        const uint32_t u = qc++;
-        const int kvh = un.hb;
+        if (barrier_or(3, NSX, *abort_flag != 0)) return false;
+        un = *desc_of(qc % C::ND);
+        if (un.nch < 0) return false;
+        u = qc++;
         if (sxid < 128) {
           // ---- Q rows -> hi + lo E4M3 terms, scaled by 2^e per row so that
           //      the row's largest |q| lands in [128, 256): for bf16 input the
@@ -806,8 +809,6 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
             e = min(7 - (static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127), 126);
           const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);  // 2^e
           if (g == 0) qscale[(u & 1u) * 16 + r] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-          // one Q buffer: every S^T MMA of the previous unit has completed,
-          // since this thread has read all of their results
           const uint32_t qb = q8;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -845,6 +846,13 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           tc5::mbar_arrive(q_empty(qslot));
         }
         named_barrier(3, NSX);  // the row scales are visible
+        return true;
+      };
+      Unit un;
+      uint32_t u = 0;
+      bool have = fetch(un, u);
+      while (have) {
+        const int kvh = un.hb;
         const int sidx = p.scale_mode == PKV_SCALE_HEAD ? kvh : 0;
         const float base_scale = p.softmax_scale * kLog2e * __ldg(p.k_scale + sidx);
         float qs[RPT], m_ref[RPT], l[RPT];
@@ -990,6 +998,11 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           if (lane == 0) tc5::mbar_arrive(p_full(c & 1u));
         }
         gc += un.nch;
+        // the next unit's Q first, so that its S^T MMAs can start while this
+        // unit's last PV drains and its partials are written
+        Unit nx;
+        uint32_t u_next = 0;
+        const bool have_next = fetch(nx, u_next);
         // ---- row sums over all keys of the unit, then the partials ----
         {
           float v[RPT];
@@ -1036,6 +1049,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           p.partial_lse[orow_of(r0 + lane)] = lr > 0.f ? (mr + fast_log2(lr)) * kLn2 : -INFINITY;
         }
         if (p.fused) fused_finish<C>(p, un, us.HB, us.RG, smem, sxid);
+        un = nx;
+        u = u_next;
+        have = have_next;
       }
     }
     // TMEM is freed once the MMAs have drained and no warp reads it
