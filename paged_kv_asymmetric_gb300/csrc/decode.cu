@@ -36,11 +36,16 @@
 //    FP8 operands are converted in registers, so the contraction runs on the
 //    warp-level m16n8k16 MMA (~4-32 flop per byte here).
 //  * bf16 cache: K and V fragments come from ldmatrix (.trans for V) on the
-//    swizzled slot.  fp8 cache: E4M3 codes become f16 in registers (exact),
-//    K through 16-byte loads with the reduction index permuted identically
-//    in Q and K, V by byte-permuting four keys' 16-column runs into k-pairs;
-//    the MMA runs in f16 with Q converted bf16 -> f16; k_scale is folded into
-//    the softmax scale and v_scale into the output.
+//    swizzled slot.  fp8 cache in the warp-MMA form (V before K in the row):
+//    E4M3 codes become f16 in registers (exact), K through 16-byte loads with
+//    the reduction index permuted identically in Q and K, V by byte-permuting
+//    four keys' 16-column runs into k-pairs; the MMA runs in f16 with Q
+//    converted bf16 -> f16; k_scale is folded into the softmax scale and
+//    v_scale into the output.
+//  * fp8 cache, K192 / V128 with K first: the tensor-core form (its branch
+//    of the kernel describes it): 128-key chunks of one head; S^T = K Q^T on
+//    tcgen05's 8-bit path with Q split exactly into two E4M3 terms, O^T +=
+//    V^T P^T in f16, both accumulators in TMEM.
 //  * Online softmax in registers with exp2.  The last chunk of a unit has its
 //    rows past the last visible key zeroed in shared memory, so garbage in a
 //    partly filled page cannot reach the MMA; the scores of those keys are
