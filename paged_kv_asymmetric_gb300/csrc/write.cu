@@ -39,6 +39,35 @@ __device__ __forceinline__ uint16_t enc2(float a, float b, float s) {
       __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
+// x / s rounded to nearest even in binary32, from y = RN(1 / s): Markstein's
+// correction (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the "Handbook
+// of Floating-Point Arithmetic", Muller et al., gives it as a theorem): with
+// q0 = RN(x y) within an ulp of x / s and the exact remainder r = x - q0 s
+// (one FMA), RN(q0 + r y) is the correctly rounded quotient, barring
+// overflow and underflow on the way.  The remainder is formed with the
+// opposite sign, r' = q0 s - x, and the quotient as q0 - r' y: the same
+// value, but a zero quotient keeps its sign (x = -0 gives -0 + -0, where
+// q0 + r y would give +0; a q0 that underflowed to zero gives x y rounded
+// with its own sign).  A non-finite q0 (x infinite or NaN) is passed through,
+// as the division gives it.  A quotient in the binary32 subnormal range may
+// differ from the division in its last bits, which no E4M3 code can see
+// (they all encode as a signed zero).  Callers take this path only for
+// scales within [2^-64, 2^64] whose reciprocal is finite and nonzero.
+__device__ __forceinline__ float div_rn_by(float x, float s, float y) {
+  const float q0 = x * y;
+  const float rn = fmaf(q0, s, -x);
+  const float q = fmaf(-rn, y, q0);
+  return isfinite(q0) ? q : q0;
+}
+
+// E4M3 of x / s with the quotient from div_rn_by (y = RN(1 / s)).
+__device__ __forceinline__ uint16_t enc2_by(float a, float b, float s, float y) {
+  float2 v = make_float2(div_rn_by(a, s, y), div_rn_by(b, s, y));
+  return static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+}
+
 // Vector path: one warp per token.  The token's slot and cache-row offsets
 // are computed once; its K and V rows of all KV heads are pieces of EPT
 // elements (16 bytes of bf16 source; EPT 8 for a bf16 cache, 16 for fp8 so
@@ -123,6 +152,108 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Token path: one warp per token, the token's pieces dealt to lanes as in
+// the vector path, but with each lane's piece geometry (source and
+// destination offsets, K or V, scale) computed once for all tokens, which
+// takes at most 32 * PPL pieces per token.  A token's loads do not wait for
+// its slot: they are issued first, and the slot decides the stores.
+template <bool FP8, int EPT, int PPL>
+__global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 : 8)) ? 3 : 1)
+    cache_write_tok_kernel(WriteParams p) {
+  constexpr int NV = EPT / 8;  // 16-byte source loads per piece
+  const int lane = threadIdx.x & 31;
+  const int kp = p.head_size / EPT;
+  const int vp = p.has_value ? p.head_size_v / EPT : 0;
+  const int per_head = kp + vp;
+  const int npieces = p.num_kv_heads * per_head;
+  const int64_t nslots = static_cast<int64_t>(p.num_blocks) * p.block_size;
+  const int64_t R = p.row_elems;
+  // offsets within one token's K / V rows and within one slot's rows (the
+  // launcher checks that they fit in 32 bits)
+  int32_t soff[PPL], doff[PPL];
+  bool is_k[PPL], act[PPL];
+  float sc[PPL], rc[PPL];  // fp8: the scale and its reciprocal RN(1 / s) (0: divide)
+#pragma unroll
+  for (int j = 0; j < PPL; ++j) {
+    const int piece = lane + 32 * j;
+    act[j] = piece < npieces;
+    const int h = act[j] ? piece / per_head : 0;
+    const int q = piece - h * per_head;
+    is_k[j] = q < kp;
+    const int e0 = (is_k[j] ? q : q - kp) * EPT;
+    soff[j] = static_cast<int32_t>((is_k[j] ? h * p.key_head_stride : h * p.val_head_stride) + e0);
+    doff[j] = static_cast<int32_t>((p.layout == PKV_NHD ? h * R : h * p.block_size * R) +
+                                   (is_k[j] ? p.k_off : p.v_off) + e0);
+    sc[j] = 1.f;
+    rc[j] = 0.f;
+    if constexpr (FP8) {
+      sc[j] = scale_for(is_k[j] ? p.k_scale : p.v_scale, p.scale_mode, h);
+      const float y = __frcp_rn(sc[j]);
+      // the FMA-corrected product where the scale and its reciprocal are
+      // finite and nonzero and the remainder cannot underflow; else divide
+      rc[j] = (isfinite(sc[j]) && isfinite(y) && y != 0.f && fabsf(sc[j]) >= 0x1p-64f &&
+               fabsf(sc[j]) <= 0x1p64f)
+                  ? y
+                  : 0.f;
+    }
+  }
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       t < p.num_tokens; t += warps) {
+    const int64_t slot = __ldg(p.slot_mapping + t);
+    const __nv_bfloat16* kt = p.key + t * p.key_tok_stride;
+    const __nv_bfloat16* vt = p.has_value ? p.value + t * p.val_tok_stride : kt;
+    uint4 v[PPL][NV];
+#pragma unroll
+    for (int j = 0; j < PPL; ++j)
+      if (act[j]) {
+        const uint4* src = reinterpret_cast<const uint4*>((is_k[j] ? kt : vt) + soff[j]);
+#pragma unroll
+        for (int c = 0; c < NV; ++c) v[j][c] = __ldg(src + c);
+      }
+    if (slot < 0) continue;
+    if (slot >= nslots) {
+      if (lane == 0) set_dev_error(p.err, PKV_EDEV_RANGE);
+      continue;
+    }
+    const int64_t blk = slot / p.block_size;
+    const int64_t off = slot - blk * p.block_size;
+    const int64_t base = p.layout == PKV_NHD
+                             ? slot * p.num_kv_heads * R
+                             : (blk * p.num_kv_heads * p.block_size + off) * R;
+#pragma unroll
+    for (int j = 0; j < PPL; ++j) {
+      if (!act[j]) continue;
+      const int64_t dst = base + doff[j];
+      if constexpr (!FP8) {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.cache) + dst) = v[j][0];
+      } else {
+        uint32_t w[EPT / 4];
+#pragma unroll
+        for (int c = 0; c < NV; ++c) {
+          const uint32_t in[4] = {v[j][c].x, v[j][c].y, v[j][c].z, v[j][c].w};
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[2 * k]));
+            float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[2 * k + 1]));
+            if (rc[j] != 0.f)
+              w[2 * c + k] = static_cast<uint32_t>(enc2_by(f0.x, f0.y, sc[j], rc[j])) |
+                             (static_cast<uint32_t>(enc2_by(f1.x, f1.y, sc[j], rc[j])) << 16);
+            else
+              w[2 * c + k] = static_cast<uint32_t>(enc2(f0.x, f0.y, sc[j])) |
+                             (static_cast<uint32_t>(enc2(f1.x, f1.y, sc[j])) << 16);
+          }
+        }
+        uint8_t* out = static_cast<uint8_t*>(p.cache) + dst;
+        if constexpr (EPT == 16)
+          *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
+        else
+          *reinterpret_cast<uint2*>(out) = make_uint2(w[0], w[1]);
+      }
+    }
+  }
+}
+
 // Element path for shapes or strides the vector path cannot take.
 template <bool FP8>
 __global__ void __launch_bounds__(256)
@@ -196,7 +327,39 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
   const int64_t tok_cap = static_cast<int64_t>(num_sms) * 16;
   const unsigned vgrid = static_cast<unsigned>(
       tok_blocks < tok_cap ? (tok_blocks > 0 ? tok_blocks : 1) : tok_cap);
-  if (!fp8 && vec_ok(8)) {
+  // token path: one warp per token, every token its own warp (the block
+  // scheduler balances), when a token's pieces fit 32 x PPL lanes
+  const int ept = fp8 ? (vec_ok(16) ? 16 : 8) : 8;
+  const int pieces = p.num_kv_heads * (p.head_size / ept +
+                                       (p.has_value ? p.head_size_v / ept : 0));
+  const int64_t tblocks64 = (static_cast<int64_t>(p.num_tokens) + 7) / 8;
+  const unsigned tgrid = static_cast<unsigned>(
+      tblocks64 < (int64_t{1} << 30) ? (tblocks64 > 0 ? tblocks64 : 1) : (int64_t{1} << 30));
+  // the token path keeps per-lane offsets in 32 bits: a token's K / V rows
+  // and a slot's rows of all heads must span less than 2^31 elements
+  const int64_t src_span = static_cast<int64_t>(p.num_kv_heads) *
+      (p.key_head_stride > p.val_head_stride ? p.key_head_stride : p.val_head_stride) +
+      p.head_size + p.head_size_v;
+  const int64_t dst_span = static_cast<int64_t>(p.num_kv_heads) * p.block_size * p.row_elems;
+  const bool tok = (fp8 ? vec_ok(ept) : vec_ok(8)) && pieces <= 512 &&
+                   src_span < (int64_t{1} << 31) && dst_span < (int64_t{1} << 31);
+  if (tok) {
+    if (!fp8) {
+      if (pieces <= 128) cache_write_tok_kernel<false, 8, 4><<<tgrid, threads, 0, stream>>>(p);
+      else if (pieces <= 160) cache_write_tok_kernel<false, 8, 5><<<tgrid, threads, 0, stream>>>(p);
+      else if (pieces <= 256) cache_write_tok_kernel<false, 8, 8><<<tgrid, threads, 0, stream>>>(p);
+      else cache_write_tok_kernel<false, 8, 16><<<tgrid, threads, 0, stream>>>(p);
+    } else if (ept == 16) {
+      if (pieces <= 96) cache_write_tok_kernel<true, 16, 3><<<tgrid, threads, 0, stream>>>(p);
+      else if (pieces <= 128) cache_write_tok_kernel<true, 16, 4><<<tgrid, threads, 0, stream>>>(p);
+      else if (pieces <= 256) cache_write_tok_kernel<true, 16, 8><<<tgrid, threads, 0, stream>>>(p);
+      else cache_write_tok_kernel<true, 16, 16><<<tgrid, threads, 0, stream>>>(p);
+    } else {
+      if (pieces <= 128) cache_write_tok_kernel<true, 8, 4><<<tgrid, threads, 0, stream>>>(p);
+      else if (pieces <= 256) cache_write_tok_kernel<true, 8, 8><<<tgrid, threads, 0, stream>>>(p);
+      else cache_write_tok_kernel<true, 8, 16><<<tgrid, threads, 0, stream>>>(p);
+    }
+  } else if (!fp8 && vec_ok(8)) {
     cache_write_vec_kernel<false, 8><<<vgrid, threads, 0, stream>>>(p);
   } else if (fp8 && vec_ok(16)) {
     cache_write_vec_kernel<true, 16><<<vgrid, threads, 0, stream>>>(p);

@@ -79,11 +79,17 @@ def test_write_strided_sources_and_k_only():
     assert (dw2.cache.data.cpu().numpy() == exp).all()
 
 
-@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.7e-3])
+# Scales with exact and inexact reciprocals, the largest binary32
+# significand below 2, powers of two at the ends of the range where the
+# write divides through the corrected reciprocal (2^-60, 2^60), and scales
+# outside it, where it divides directly (1e-30, 1e30).
+@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.7e-3, 1.0 / 3.0, 0.3, 7.0,
+                                   float(np.float32(1.9999999)), 2.0 ** -60,
+                                   2.0 ** 60, 1e-30, 1e30])
 def test_fp8_encode_every_bf16_pattern(scale):
     """All 65,536 bf16 bit patterns through the fp8 write, bit-exact against
-    the oracle's E4M3 encoder; NaN inputs must give a NaN code on both
-    sides (either sign)."""
+    the oracle's E4M3 encoder (x / s divided in binary32); NaN inputs must
+    give a NaN code on both sides (either sign)."""
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     H, dk, dv = 4, 192, 128
     per_tok = H * (dk + dv)
