@@ -74,9 +74,9 @@ def _load():
         lib.oracle_kv_cache_write.restype = i32
         lib.oracle_paged_attn.argtypes = [
             P, i32, i32, P, ctypes.POINTER(CacheDesc), P, i32, P, P, i32,
-            ctypes.c_float, P, P, P, i32, i32, i32, P, P]
+            ctypes.c_float, P, P, P, i32, i32, i32, P, P, P]
         lib.oracle_paged_attn.restype = i32
-        lib.oracle_splitkv_reduce.argtypes = [P, P, i32, i64, i32, P, P]
+        lib.oracle_splitkv_reduce.argtypes = [P, P, i32, i64, i32, P, P, P, i32]
         lib.oracle_splitkv_reduce.restype = None
         _lib = lib
         return lib
@@ -146,11 +146,13 @@ def kv_cache_write(key_bits, value_bits, slot_mapping, cache, d: CacheDesc,
 def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
                seq_lens, query_start_loc, softmax_scale, k_scale=None,
                v_scale=None, tokens=None, num_splits=0, split=-1,
-               threads=1):
+               threads=1, sinks=None):
     """Returns (out [n, Hq, dv] float64, lse [n, Hq] float64) for the query
     tokens listed in ``tokens`` (all tokens when None).  ``threads`` > 1
     splits the token list over Python threads (the C call releases the
-    GIL); the arithmetic of each row is unchanged."""
+    GIL); the arithmetic of each row is unchanged.  ``sinks`` (float32 [Hq],
+    or None): one attention-sink logit per query head, for whole rows
+    (split < 0) only."""
     lib = _load()
     q_bits = _c(q_bits, np.uint16)
     T = q_bits.shape[0]
@@ -160,6 +162,8 @@ def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
     kscale = None if k_scale is None else _c(k_scale, np.float32)
     vscale = None if v_scale is None else _c(v_scale, np.float32)
     toks = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    snk = None if sinks is None else _c(sinks, np.float32)
+    assert snk is None or snk.shape == (num_q_heads,)
     n = int(toks.shape[0])
     out = np.zeros((n, num_q_heads, d.head_size_v), dtype=np.float64)
     lse = np.zeros((n, num_q_heads), dtype=np.float64)
@@ -176,7 +180,7 @@ def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
             _ptr(q_bits), num_q_heads, T, _ptr(cache), ctypes.byref(d),
             _ptr(bt), max_blocks, _ptr(sl), _ptr(qsl), int(sl.shape[0]),
             float(softmax_scale), _ptr(kscale), _ptr(vscale), _ptr(sub),
-            hi - lo, int(num_splits), int(split), _ptr(o), _ptr(ls))
+            hi - lo, int(num_splits), int(split), _ptr(o), _ptr(ls), _ptr(snk))
 
     if threads <= 1 or n < 2:
         rcs = [run(0, n)]
@@ -197,15 +201,18 @@ def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
     return out, lse
 
 
-def splitkv_reduce(partial_o, partial_lse):
+def splitkv_reduce(partial_o, partial_lse, sinks=None, num_q_heads=1):
     """partial_o [S, rows, dv] float32, partial_lse [S, rows] float32 ->
-    (out [rows, dv] float64, lse [rows] float64)."""
+    (out [rows, dv] float64, lse [rows] float64).  ``sinks`` (float32
+    [num_q_heads], or None): row r's sink logit is sinks[r % num_q_heads]."""
     lib = _load()
     po = _c(partial_o, np.float32)
     pl = _c(partial_lse, np.float32)
     S, rows, dv = po.shape
+    snk = None if sinks is None else _c(sinks, np.float32)
+    assert snk is None or snk.shape == (num_q_heads,)
     out = np.zeros((rows, dv), dtype=np.float64)
     lse = np.zeros((rows,), dtype=np.float64)
     lib.oracle_splitkv_reduce(_ptr(po), _ptr(pl), S, rows, dv, _ptr(out),
-                              _ptr(lse))
+                              _ptr(lse), _ptr(snk), int(num_q_heads))
     return out, lse

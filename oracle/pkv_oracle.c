@@ -23,7 +23,9 @@
  *              "diffbot/MiMo-V2.6-Flash-MOPD-FP8KV-W4A8-2x-RTX-PRO-6000",
  *              sections "What the kernels do" (split-KV for the verify step,
  *              FP8 E4M3 K/V) and "Update 2026-10-01" (rows with no visible
- *              keys give 0, not NaN, in the split-KV reducer).
+ *              keys give 0, not NaN, in the split-KV reducer; the attention
+ *              sink taken as one extra logit in the softmax denominator,
+ *              vLLM #58235).
  *
  * Precision: the FP8 encode divides in IEEE binary32 (that division decides
  * the code byte, and the GPU takes the same decision in the same precision);
@@ -229,24 +231,31 @@ static double cache_read(const void *cache, const oracle_cache_desc *d,
  * out[0 .. dv) = sum_j softmax_j * V_j and *lse = m + log(sum exp(s_j - m)),
  * computed in two passes (max, then sums).  No visible key: out = 0 and
  * lse = -inf ([MiMo-2xRTX] "Update 2026-10-01": such rows are 0, never NaN).
+ *
+ * Attention sink ([MiMo-2xRTX] "Update 2026-10-01", vLLM #58235: the sink is
+ * an extra softmax-denominator logit): `sink` is one more logit with no value
+ * vector, out = sum_j exp(s_j) V_j / (exp(sink) + sum_j exp(s_j)) and
+ * lse = log(exp(sink) + sum_j exp(s_j)).  sink = -inf is no sink.  With a
+ * finite sink a row without visible keys is 0 with lse = sink.
  */
 static void attend_row(const uint16_t *q_row, const void *cache,
                        const oracle_cache_desc *d, const int32_t *bt_row,
                        int64_t key_lo, int64_t key_hi, int g, double scale,
-                       double ks, double vs, double *out, double *lse)
+                       double ks, double vs, double sink, double *out,
+                       double *lse)
 {
     int64_t j;
     int i;
-    double m = -INFINITY, l = 0.0;
+    double m = sink, l;
     int dk = d->head_size, dv = d->head_size_v;
 
     for (i = 0; i < dv; ++i)
         out[i] = 0.0;
     if (key_hi <= key_lo) {
-        *lse = -INFINITY;
+        *lse = sink;
         return;
     }
-    /* pass 1: the row maximum of the scaled scores */
+    /* pass 1: the row maximum of the scaled scores (and the sink) */
     for (j = key_lo; j < key_hi; ++j) {
         int64_t row = row_offset_elems(d, bt_row[j / d->block_size],
                                        j % d->block_size, g);
@@ -258,7 +267,9 @@ static void attend_row(const uint16_t *q_row, const void *cache,
         if (s > m)
             m = s;
     }
-    /* pass 2: exponentials, their sum and the weighted sum of V */
+    /* pass 2: exponentials, their sum (the sink's term first) and the
+     * weighted sum of V */
+    l = exp(sink - m);
     for (j = key_lo; j < key_hi; ++j) {
         int64_t row = row_offset_elems(d, bt_row[j / d->block_size],
                                        j % d->block_size, g);
@@ -284,14 +295,17 @@ static void attend_row(const uint16_t *q_row, const void *cache,
  * bf16 (raw bits), out_o is [n][Hq][dv] and out_lse is [n][Hq], binary64.
  * split < 0 computes the whole row; otherwise the partial of segment
  * `split` of `num_splits` (see attend_row).  Returns 0, or -1 when a token
- * index is outside every sequence. */
+ * index is outside every sequence.  sinks (NULL: none) holds one sink logit
+ * per query head; it enters whole rows only (split < 0): a segment's partial
+ * is sink-free and the merge adds the sink once. */
 int oracle_paged_attn(const uint16_t *q, int num_q_heads, int num_tokens,
                       const void *cache, const oracle_cache_desc *d,
                       const int32_t *block_table, int max_blocks_per_seq,
                       const int32_t *seq_lens, const int32_t *query_start_loc,
                       int num_seqs, float softmax_scale, const float *k_scale,
                       const float *v_scale, const int32_t *tokens, int n_tokens,
-                      int num_splits, int split, double *out_o, double *out_lse)
+                      int num_splits, int split, double *out_o, double *out_lse,
+                      const float *sinks)
 {
     int n = tokens ? n_tokens : num_tokens;
     int G = num_q_heads / d->num_kv_heads;
@@ -334,6 +348,7 @@ int oracle_paged_attn(const uint16_t *q, int num_q_heads, int num_tokens,
                        d, bt_row, lo, hi, g, (double)softmax_scale,
                        (double)scale_of(k_scale, d->scale_mode, g),
                        (double)scale_of(v_scale, d->scale_mode, g),
+                       (sinks && split < 0) ? (double)sinks[h] : -INFINITY,
                        out_o + ((int64_t)k * num_q_heads + h) * d->head_size_v,
                        out_lse + (int64_t)k * num_q_heads + h);
         }
@@ -349,15 +364,20 @@ int oracle_paged_attn(const uint16_t *q, int num_q_heads, int num_tokens,
  * the row is 0 with lse -inf.  Otherwise w_s = exp(lse_s - M) (0 for empty
  * segments), out = sum_s w_s * o_s / sum_s w_s and lse = M + log(sum_s w_s).
  * partial_o is [S][rows][dv] and partial_lse [S][rows] (binary32, the
- * library's partial format); o_s of an empty segment is never read. */
+ * library's partial format); o_s of an empty segment is never read.
+ * sinks (NULL: none): the sink logit of row r is sinks[r % num_q_heads] (rows
+ * are (token, query head) pairs); it joins the merge as one more segment
+ * with lse = sink and o = 0, so M also covers it and W gains exp(sink - M):
+ * a row whose segments are all empty is then 0 with lse = sink. */
 void oracle_splitkv_reduce(const float *partial_o, const float *partial_lse,
                            int num_splits, int64_t rows, int dv, double *out,
-                           double *lse_out)
+                           double *lse_out, const float *sinks, int num_q_heads)
 {
     int64_t r;
     int s, i;
     for (r = 0; r < rows; ++r) {
-        double M = -INFINITY, W = 0.0;
+        double sink = sinks ? (double)sinks[r % num_q_heads] : -INFINITY;
+        double M = sink, W;
         double *o = out + r * dv;
         for (i = 0; i < dv; ++i)
             o[i] = 0.0;
@@ -370,6 +390,7 @@ void oracle_splitkv_reduce(const float *partial_o, const float *partial_lse,
             lse_out[r] = -INFINITY;
             continue;
         }
+        W = exp(sink - M);
         for (s = 0; s < num_splits; ++s) {
             double x = partial_lse[(int64_t)s * rows + r];
             double w;
