@@ -256,10 +256,20 @@ def gpu_arm(args, ws, rank, local):
     sub = {}
     reps = max(3, args.sub_reps)
 
-    def attn_decode_sub(name, wk, splits):
+    def attn_decode_sub(name, wk, splits, time_write=False):
         dwk = wl.to_device(wk, device=dev)
-        pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
-                           dwk.k_scale, dwk.v_scale)
+
+        def wr():
+            pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
+                               dwk.k_scale, dwk.v_scale)
+        wr()
+        wsub = {}
+        if time_write:  # the whole context's cache write (e.g. the fp8 encode)
+            mw, _ = time_launches(wr, reps, 2, flush)
+            nw = int(dwk.k_ctx.shape[0])
+            wb = write_bytes(wk, nw)
+            wsub = {"write_ms": mw, "write_bytes": wb, "write_GBps": wb / (mw * 1e-3) / 1e9,
+                    "write_frac_hbm": wb / (mw * 1e-3) / 1e9 / hbm}
         Tk, Hk, dvk = wk.num_tokens, wk.num_q_heads, wk.head_size_v
         pok = torch.empty(splits, Tk, Hk, dvk, dtype=torch.float32, device=dev)
         plk = torch.empty(splits, Tk, Hk, dtype=torch.float32, device=dev)
@@ -280,7 +290,7 @@ def gpu_arm(args, ws, rank, local):
         sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
                      "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
                      "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
-                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm}
+                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm, **wsub}
         del dwk, pok, plk, outk
         torch.cuda.empty_cache()
 
@@ -317,7 +327,7 @@ def gpu_arm(args, ws, rank, local):
         if args.only == "prefill":
             prefill_sub(f"prefill_{args.prefill_tokens}", args.prefill_tokens)
         elif args.only == "verify":
-            attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), 16)
+            attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), 16, time_write=True)
         elif args.only == "mla":
             s = pkv.decode_suggest_splits(1, 16, 1, 1, 100000, 64)
             attn_decode_sub("mla_b1_h16", wl.mla_decode(batch=1, heads=16,
@@ -460,7 +470,7 @@ def gpu_arm(args, ws, rank, local):
             if args.long:
                 prefill_sub("prefill_128k", 131072)
         wv = wl.verify_fp8(device=dev)
-        attn_decode_sub("verify_fp8", wv, 16)
+        attn_decode_sub("verify_fp8", wv, 16, time_write=True)
         del wv
         for b in (1, 16):
             for h in (12, 16):

@@ -161,6 +161,26 @@ int pkv_paged_attn_prefill(const void *q, int num_q_heads, int num_tokens,
                            pkv_stream_t stream);
 
 /*
+ * pkv_paged_attn_prefill_sink -- pkv_paged_attn_prefill with an attention
+ * sink: one extra logit per query head in every row's softmax denominator,
+ * with no value vector (MiMo model card, "Update 2026-10-01": the vision
+ * encoder's sink, vLLM #58235):
+ *   out = sum_j exp(s_j) V_j / (exp(sinks[h]) + sum_j exp(s_j)),
+ * s_j = softmax_scale * q.k_j over the row's visible keys, h the row's query
+ * head.  sinks: float32 [num_q_heads], device memory; a sink of -inf is no
+ * sink; NULL gives pkv_paged_attn_prefill's result.  Other arguments,
+ * layouts, status codes and supported shapes as in pkv_paged_attn_prefill.
+ */
+int pkv_paged_attn_prefill_sink(const void *q, int num_q_heads, int num_tokens,
+                                const void *cache, const pkv_cache_desc *d,
+                                const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *seq_lens,
+                                const int32_t *query_start_loc, int num_seqs,
+                                float softmax_scale, const float *k_scale,
+                                const float *v_scale, const float *sinks,
+                                void *out, pkv_stream_t stream);
+
+/*
  * pkv_paged_attn_decode -- split-KV decode and speculative verify (q_len 1
  * .. max_query_len) over the paged cache: the verify-step split-KV of the
  * MiMo model card's "What the kernels do", the 12-head MLA decode of vLLM
@@ -287,6 +307,29 @@ int pkv_paged_attn_decode_fused_noalloc(const void *q, int num_q_heads,
 int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
                        int num_splits, int num_rows, int head_size_v,
                        void *out, float *lse_out, pkv_stream_t stream);
+
+/*
+ * pkv_splitkv_reduce_sink -- pkv_splitkv_reduce with an attention sink: one
+ * extra logit per query head in the softmax denominator, with no value
+ * vector (MiMo model card, "Update 2026-10-01": the vision encoder's sink,
+ * vLLM #58235).  Row r is (token r / num_q_heads, query head r %
+ * num_q_heads), as in the decode's partials, and its sink is
+ * sinks[r % num_q_heads].  The sink enters the merge once per row, as one
+ * more segment with lse = sink and o = 0:
+ *   M = max(sink, max_s lse_s); W = exp(sink - M) + sum_s exp(lse_s - M);
+ *   out = sum_s exp(lse_s - M) o_s / W; lse_out = M + log(W).
+ * A row whose segments are all empty is then 0 with lse = sink.  The decode
+ * partials themselves carry no sink: pkv_paged_attn_decode followed by this
+ * call gives sink attention.
+ * sinks: float32 [num_q_heads], device memory, or NULL (then the result is
+ * pkv_splitkv_reduce's); a sink of -inf is no sink.
+ * PKV_EINVAL also when num_q_heads < 1 or num_rows is not a multiple of it.
+ * Other arguments and status codes as in pkv_splitkv_reduce.
+ */
+int pkv_splitkv_reduce_sink(const float *partial_o, const float *partial_lse,
+                            int num_splits, int num_rows, int head_size_v,
+                            const float *sinks, int num_q_heads, void *out,
+                            float *lse_out, pkv_stream_t stream);
 
 /*
  * pkv_decode_suggest_splits -- a split count for the decode launch on the

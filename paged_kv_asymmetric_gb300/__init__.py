@@ -34,7 +34,8 @@ SCALE_NONE, SCALE_TENSOR, SCALE_HEAD = 0, 1, 2
 EXPORTED = (
     "pkv_kv_cache_write", "pkv_paged_attn_prefill", "pkv_paged_attn_decode",
     "pkv_paged_attn_decode_fused", "pkv_paged_attn_decode_fused_noalloc",
-    "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_decode_suggest_splits",
+    "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_splitkv_reduce_sink",
+    "pkv_paged_attn_prefill_sink", "pkv_decode_suggest_splits",
     "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
@@ -101,6 +102,9 @@ def _lib():
         lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_splitkv_reduce.argtypes = [P, P, I, I, I, P, P, P]
+        lib.pkv_splitkv_reduce_sink.argtypes = [P, P, I, I, I, P, I, P, P, P]
+        lib.pkv_paged_attn_prefill_sink.argtypes = [P, I, I, P, D, P, I, P, P, I,
+                                                    F, P, P, P, P, P]
         lib.pkv_decode_suggest_splits.argtypes = [I, I, I, I, I, I]
         lib.pkv_supports.argtypes = [I, I, I]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
@@ -181,18 +185,27 @@ def _attn_common(q, block_table, seq_lens, query_start_loc):
 
 def paged_attn_prefill(q, cache: Cache, block_table, seq_lens,
                        query_start_loc, softmax_scale, out=None,
-                       k_scale=None, v_scale=None, stream=None):
-    """q: bf16 [T, Hq, dk]; returns out bf16 [T, Hq, dv]."""
+                       k_scale=None, v_scale=None, stream=None, sinks=None):
+    """q: bf16 [T, Hq, dk]; returns out bf16 [T, Hq, dv].  ``sinks``: float32
+    [Hq] CUDA tensor of attention-sink logits (pkv_paged_attn_prefill_sink),
+    or None."""
     _attn_common(q, block_table, seq_lens, query_start_loc)
     T, Hq, _ = q.shape
     if out is None:
         out = torch.empty(T, Hq, cache.desc.head_size_v, dtype=torch.bfloat16,
                           device=q.device)
-    _check("pkv_paged_attn_prefill", _lib().pkv_paged_attn_prefill(
-        _ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
-        _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
-        _ptr(query_start_loc), int(seq_lens.shape[0]), float(softmax_scale),
-        _ptr(k_scale), _ptr(v_scale), _ptr(out), _stream(stream)))
+    args = (_ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
+            _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+            _ptr(query_start_loc), int(seq_lens.shape[0]), float(softmax_scale),
+            _ptr(k_scale), _ptr(v_scale))
+    if sinks is None:
+        _check("pkv_paged_attn_prefill", _lib().pkv_paged_attn_prefill(
+            *args, _ptr(out), _stream(stream)))
+    else:
+        assert sinks.dtype == torch.float32 and sinks.is_contiguous()
+        assert tuple(sinks.shape) == (Hq,)
+        _check("pkv_paged_attn_prefill_sink", _lib().pkv_paged_attn_prefill_sink(
+            *args, _ptr(sinks), _ptr(out), _stream(stream)))
     return out
 
 
@@ -290,9 +303,11 @@ def paged_attn_decode_fused_noalloc(q, cache: Cache, block_table, seq_lens,
 
 
 def splitkv_reduce(partial_o, partial_lse, out=None, lse_out=None,
-                   stream=None):
+                   stream=None, sinks=None):
     """partial_o [S, ..., dv] f32, partial_lse [S, ...] f32 -> out bf16
-    [..., dv] (and lse_out f32 [...] when given)."""
+    [..., dv] (and lse_out f32 [...] when given).  ``sinks``: float32 [Hq]
+    CUDA tensor of attention-sink logits, Hq the last dimension of the rows
+    (pkv_splitkv_reduce_sink), or None."""
     assert partial_o.dtype == torch.float32 and partial_o.is_contiguous()
     assert partial_lse.dtype == torch.float32 and partial_lse.is_contiguous()
     S = partial_o.shape[0]
@@ -303,9 +318,17 @@ def splitkv_reduce(partial_o, partial_lse, out=None, lse_out=None,
     if out is None:
         out = torch.empty(*partial_o.shape[1:], dtype=torch.bfloat16,
                           device=partial_o.device)
-    _check("pkv_splitkv_reduce", _lib().pkv_splitkv_reduce(
-        _ptr(partial_o), _ptr(partial_lse), S, rows, dv, _ptr(out),
-        _ptr(lse_out), _stream(stream)))
+    if sinks is None:
+        _check("pkv_splitkv_reduce", _lib().pkv_splitkv_reduce(
+            _ptr(partial_o), _ptr(partial_lse), S, rows, dv, _ptr(out),
+            _ptr(lse_out), _stream(stream)))
+    else:
+        assert sinks.dtype == torch.float32 and sinks.is_contiguous()
+        hq = int(sinks.shape[0])
+        assert partial_lse.shape[-1] == hq
+        _check("pkv_splitkv_reduce_sink", _lib().pkv_splitkv_reduce_sink(
+            _ptr(partial_o), _ptr(partial_lse), S, rows, dv, _ptr(sinks), hq,
+            _ptr(out), _ptr(lse_out), _stream(stream)))
     return out
 
 

@@ -194,14 +194,14 @@ int pkv_kv_cache_write(const void* key, int64_t key_tok_stride,
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }
 
-int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
-                           const void* cache, const pkv_cache_desc* d,
-                           const int32_t* block_table, int max_blocks_per_seq,
-                           const int32_t* seq_lens,
-                           const int32_t* query_start_loc, int num_seqs,
-                           float softmax_scale, const float* k_scale,
-                           const float* v_scale, void* out,
-                           pkv_stream_t stream) {
+namespace {
+
+int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cache,
+                 const pkv_cache_desc* d, const int32_t* block_table,
+                 int max_blocks_per_seq, const int32_t* seq_lens,
+                 const int32_t* query_start_loc, int num_seqs, float softmax_scale,
+                 const float* k_scale, const float* v_scale, const float* sinks,
+                 void* out, pkv_stream_t stream) {
   int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
                              max_blocks_per_seq, seq_lens, query_start_loc,
                              num_seqs, softmax_scale, k_scale, v_scale);
@@ -228,9 +228,37 @@ int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
                                   query_start_loc, num_seqs, softmax_scale,
                                   k_scale, v_scale, err);
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.sinks = sinks;
   cudaError_t e = pkv::launch_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
+                           const void* cache, const pkv_cache_desc* d,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* seq_lens,
+                           const int32_t* query_start_loc, int num_seqs,
+                           float softmax_scale, const float* k_scale,
+                           const float* v_scale, void* out,
+                           pkv_stream_t stream) {
+  return prefill_impl(q, num_q_heads, num_tokens, cache, d, block_table, max_blocks_per_seq,
+                      seq_lens, query_start_loc, num_seqs, softmax_scale, k_scale, v_scale,
+                      nullptr, out, stream);
+}
+
+int pkv_paged_attn_prefill_sink(const void* q, int num_q_heads, int num_tokens,
+                                const void* cache, const pkv_cache_desc* d,
+                                const int32_t* block_table, int max_blocks_per_seq,
+                                const int32_t* seq_lens, const int32_t* query_start_loc,
+                                int num_seqs, float softmax_scale, const float* k_scale,
+                                const float* v_scale, const float* sinks, void* out,
+                                pkv_stream_t stream) {
+  return prefill_impl(q, num_q_heads, num_tokens, cache, d, block_table, max_blocks_per_seq,
+                      seq_lens, query_start_loc, num_seqs, softmax_scale, k_scale, v_scale,
+                      sinks, out, stream);
 }
 
 namespace {
@@ -450,6 +478,28 @@ int pkv_splitkv_reduce(const float* partial_o, const float* partial_lse,
       partial_o, partial_lse, num_splits, num_rows, head_size_v,
       static_cast<__nv_bfloat16*>(out), lse_out,
       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_splitkv_reduce_sink(const float* partial_o, const float* partial_lse,
+                            int num_splits, int num_rows, int head_size_v,
+                            const float* sinks, int num_q_heads, void* out, float* lse_out,
+                            pkv_stream_t stream) {
+  if (num_splits < 0 || num_rows < 0 || head_size_v < 1 || num_q_heads < 1)
+    return PKV_EINVAL;
+  if (num_rows % num_q_heads != 0) return PKV_EINVAL;
+  if (num_rows == 0) return PKV_OK;
+  if (out == nullptr) return PKV_EINVAL;
+  if (num_splits > 0 && (partial_o == nullptr || partial_lse == nullptr))
+    return PKV_EINVAL;
+  if ((head_size_v & 3) == 0 &&
+      ((reinterpret_cast<uintptr_t>(partial_o) & 15u) != 0 ||
+       (reinterpret_cast<uintptr_t>(out) & 7u) != 0))
+    return PKV_EINVAL;
+  cudaError_t e = pkv::launch_splitkv_reduce(
+      partial_o, partial_lse, num_splits, num_rows, head_size_v,
+      static_cast<__nv_bfloat16*>(out), lse_out, reinterpret_cast<cudaStream_t>(stream),
+      sinks, num_q_heads);
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }
 

@@ -56,6 +56,9 @@ struct AttnParams {
   int* counters;
   float* lse_out;
   int fused;
+  // prefill: one attention-sink logit per query head (nullable), an extra
+  // term exp(sink) in each row's softmax denominator
+  const float* sinks;
 };
 
 // The fused decode merges in-kernel up to this many splits (its per-row
@@ -69,11 +72,14 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
 cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream);
 bool decode_supported(int head_size, int head_size_v, int dtype);
 
+// sinks: nullable, one attention-sink logit per query head; row r takes
+// sinks[r % num_q_heads].
 cudaError_t launch_splitkv_reduce(const float* partial_o,
                                   const float* partial_lse, int num_splits,
                                   int num_rows, int head_size_v,
                                   __nv_bfloat16* out, float* lse_out,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const float* sinks = nullptr,
+                                  int num_q_heads = 1);
 
 cudaError_t launch_prefill(const AttnParams& p, int num_sms,
                            cudaStream_t stream);

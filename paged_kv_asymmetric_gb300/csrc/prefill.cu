@@ -522,6 +522,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---- epilogue: O / l -> bf16 ----
       if (!wwait(bar(B_ODONE0 + x), items & 1u)) break;
       tc5::tc_fence_after();
+      if (p.sinks != nullptr && valid && m != -INFINITY) {
+        // the attention sink: one more logit in the denominator, no value
+        const float sk = __ldg(p.sinks + it.g * G + hr);
+        if (sk != -INFINITY) l += fast_exp2(fmaf(sk, kLog2e, -m));
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
 #pragma unroll

@@ -2,7 +2,10 @@
 // card, "What the kernels do" and "Update 2026-10-01"): each row's segment
 // partials (o_s, lse_s) are combined with weights exp(lse_s - max lse); a row
 // whose segments are all empty is written as 0 with lse -inf instead of the
-// exp(-inf - -inf) = NaN the unclamped merge produces.
+// exp(-inf - -inf) = NaN the unclamped merge produces.  An attention sink
+// (the same card's "Update 2026-10-01": one extra logit in the softmax
+// denominator, vLLM #58235) joins the merge once per row as one more segment
+// with lse = sink and no value: it enters the maximum and the weight sum.
 //
 // One warp per row: the split weights are recomputed by every lane from the
 // (broadcast) lse values, and each lane accumulates four consecutive output
@@ -21,7 +24,8 @@ __global__ void __launch_bounds__(256)
     splitkv_reduce_kernel(const float* __restrict__ po,
                           const float* __restrict__ plse, int S, int rows,
                           int dv, __nv_bfloat16* __restrict__ out,
-                          float* __restrict__ lse_out) {
+                          float* __restrict__ lse_out, const float* __restrict__ sinks,
+                          int hq) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const bool vec = (dv & 3) == 0;
@@ -33,6 +37,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
       M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float sink = sinks != nullptr ? __ldg(sinks + r % hq) : -INFINITY;
+    M = fmaxf(M, sink);
     __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
     if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
       for (int c = lane; c < dv; c += 32) orow[c] = __float2bfloat16_rn(0.f);
@@ -40,12 +46,14 @@ __global__ void __launch_bounds__(256)
       continue;
     }
     const float Ml2 = M * kLog2e;
+    // the sink's weight (0 without a sink)
+    const float wsink = sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2));
     float W = 0.f;
     if (vec) {
       for (int c0 = 0; c0 < dv; c0 += 128) {
         const int c = c0 + 4 * lane;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float wsum = 0.f;
+        float wsum = wsink;
         for (int s = 0; s < S; ++s) {
           const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
           if (x == -INFINITY) continue;  // empty segment: o_s is not read
@@ -71,7 +79,7 @@ __global__ void __launch_bounds__(256)
       }
     } else {
       for (int c = lane; c < dv; c += 32) {
-        float acc = 0.f, wsum = 0.f;
+        float acc = 0.f, wsum = wsink;
         for (int s = 0; s < S; ++s) {
           const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
           if (x == -INFINITY) continue;
@@ -102,7 +110,8 @@ __global__ void __launch_bounds__(THREADS)
     splitkv_reduce_rows_kernel(const float* __restrict__ po,
                                const float* __restrict__ plse, int S, int rows,
                                int dv, __nv_bfloat16* __restrict__ out,
-                               float* __restrict__ lse_out) {
+                               float* __restrict__ lse_out,
+                               const float* __restrict__ sinks, int hq) {
   __shared__ float red[THREADS / 32];
   __shared__ float4 part[THREADS];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -126,6 +135,8 @@ __global__ void __launch_bounds__(THREADS)
   for (int s = tid; s < S; s += THREADS)
     M = fmaxf(M, __ldg(plse + static_cast<int64_t>(s) * rows + r));
   M = block_reduce(M, true);
+  const float sink = sinks != nullptr ? __ldg(sinks + r % hq) : -INFINITY;
+  M = fmaxf(M, sink);
   __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
   const int dv4 = dv >> 2;
   const int cb4 = dv4 / ncb;  // 16-byte pieces of this block
@@ -141,7 +152,8 @@ __global__ void __launch_bounds__(THREADS)
     const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
     if (x != -INFINITY) wsum += fast_exp2(fmaf(x, kLog2e, -Ml2));
   }
-  const float W = block_reduce(wsum, false);
+  const float W = block_reduce(wsum, false) +
+                  (sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2)));
   const float inv = 1.f / W;
   const int cols = cb4 < THREADS ? cb4 : THREADS;
   const int ngrp = THREADS / cols;
@@ -200,7 +212,8 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
                                   const float* partial_lse, int num_splits,
                                   int num_rows, int head_size_v,
                                   __nv_bfloat16* out, float* lse_out,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const float* sinks,
+                                  int num_q_heads) {
   if (num_rows == 0) return cudaSuccess;
   if ((head_size_v & 3) == 0) {
     // column blocks (a power of two dividing dv/4, >= 8 pieces each) until
@@ -211,14 +224,16 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
            dv4 / (2 * ncb) >= 8)
       ncb *= 2;
     splitkv_reduce_rows_kernel<512><<<dim3(num_rows, ncb), 512, 0, stream>>>(
-        partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out);
+        partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
+        num_q_heads);
     return cudaGetLastError();
   }
   const int wpb = 8;
   int blocks = (num_rows + wpb - 1) / wpb;
   if (blocks > 65535) blocks = 65535;
   splitkv_reduce_kernel<<<blocks, 32 * wpb, 0, stream>>>(
-      partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out);
+      partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
+      num_q_heads);
   return cudaGetLastError();
 }
 
