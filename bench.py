@@ -284,13 +284,19 @@ def gpu_arm(args, ws, rank, local):
 
         def red():
             pkv.splitkv_reduce(pok, plk, out=outk)
+        sinks = torch.linspace(-2.0, 2.0, Hk, dtype=torch.float32, device=dev)
+
+        def red_sink():  # the same merge with an attention sink per head
+            pkv.splitkv_reduce(pok, plk, out=outk, sinks=sinks)
         md, _ = time_launches(dec, reps, 2, flush)
         mr, _ = time_launches(red, reps, 2, flush)
+        mrs, _ = time_launches(red_sink, reps, 2, flush)
         b = decode_bytes(wk)
         sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
                      "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
                      "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
-                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm, **wsub}
+                     "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm,
+                     "reduce_sink_ms": mrs, **wsub}
         del dwk, pok, plk, outk
         torch.cuda.empty_cache()
 
@@ -311,10 +317,18 @@ def gpu_arm(args, ws, rank, local):
                                    dwk.seq_lens, dwk.query_start_loc,
                                    wk.softmax_scale, out=outk)
         mp, _ = time_launches(pf, reps, 2, flush)
+        sinks = torch.linspace(-2.0, 2.0, wk.num_q_heads, dtype=torch.float32, device=dev)
+
+        def pf_sink():  # the same prefill with an attention sink per head
+            pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
+                                   dwk.seq_lens, dwk.query_start_loc,
+                                   wk.softmax_scale, out=outk, sinks=sinks)
+        mps, _ = time_launches(pf_sink, reps, 2, flush)
         fl = prefill_flops(wk)
         sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
                      "TFLOPs": fl / (mp * 1e-3) / 1e12,
                      "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
+                     "sink_ms": mps, "sink_TFLOPs": fl / (mps * 1e-3) / 1e12,
                      "write_ms": mw, "write_bytes": wb,
                      "write_GBps": wb / (mw * 1e-3) / 1e9,
                      "write_frac_hbm": wb / (mw * 1e-3) / 1e9 / hbm}
