@@ -335,11 +335,42 @@ def gpu_arm(args, ws, rank, local):
         del dwk, outk
         torch.cuda.empty_cache()
 
+    def prefill_fp8_sub(name, n_tokens):
+        # the same causal prefill over an FP8 E4M3 cache (per-head scales):
+        # the whole public call, the widening pass included
+        wk = wl.make_workload(f"prefill-{n_tokens}-fp8", seq_lens=[n_tokens],
+                              q_lens=[n_tokens], kv_dtype=wl.FP8,
+                              scale_mode=wl.SCALE_HEAD, seed=0, device=dev)
+        dwk = wl.to_device(wk, device=dev)
+        pkv.kv_cache_write(dwk.k_ctx, dwk.v_ctx, dwk.slots_all, dwk.cache,
+                           dwk.k_scale, dwk.v_scale)
+        outk = torch.empty(wk.num_tokens, wk.num_q_heads, wk.head_size_v,
+                           dtype=torch.bfloat16, device=dev)
+        nws = pkv.prefill_fp8_workspace_bytes(wk.num_seqs, dwk.block_table.shape[1],
+                                              dwk.cache)
+        wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+        def pf8():
+            pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
+                                   dwk.seq_lens, dwk.query_start_loc,
+                                   wk.softmax_scale, out=outk, k_scale=dwk.k_scale,
+                                   v_scale=dwk.v_scale, workspace=wsp)
+        mp, _ = time_launches(pf8, reps, 2, flush)
+        fl = prefill_flops(wk)
+        sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
+                     "TFLOPs": fl / (mp * 1e-3) / 1e12,
+                     "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
+                     "workspace_bytes": nws}
+        del dwk, outk, wsp
+        torch.cuda.empty_cache()
+
     if args.only:
         sampler = ClockSampler(local)
         sampler.start()
         if args.only == "prefill":
             prefill_sub(f"prefill_{args.prefill_tokens}", args.prefill_tokens)
+        elif args.only == "prefill_fp8":
+            prefill_fp8_sub(f"prefill_fp8_{args.prefill_tokens}", args.prefill_tokens)
         elif args.only == "verify":
             attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), 16, time_write=True)
         elif args.only == "mla":
@@ -481,6 +512,7 @@ def gpu_arm(args, ws, rank, local):
     if not args.no_sub:
         if not args.skip_prefill:
             prefill_sub("prefill_32k", 32768)
+            prefill_fp8_sub("prefill_fp8_32k", 32768)
             if args.long:
                 prefill_sub("prefill_128k", 131072)
         wv = wl.verify_fp8(device=dev)
@@ -610,7 +642,7 @@ def main(argv=None):
     ap.add_argument("--long", action="store_true", help="add the 131,072-token prefill")
     ap.add_argument("--no-sub", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "verify", "mla", "decode"],
+    ap.add_argument("--only", choices=["prefill", "prefill_fp8", "verify", "mla", "decode"],
                     help="run one sub-measurement alone (for profiling)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
     ap.add_argument("--sub-reps", type=int, default=20)

@@ -161,6 +161,50 @@ int pkv_paged_attn_prefill(const void *q, int num_q_heads, int num_tokens,
                            pkv_stream_t stream);
 
 /*
+ * pkv_prefill_fp8_workspace_bytes -- size of the workspace that
+ * pkv_paged_attn_prefill_fp8 needs: num_seqs * max_blocks_per_seq pages of
+ * block_size * num_kv_heads * row_elems bf16 elements (rounded up to 256
+ * bytes), then num_seqs * max_blocks_per_seq int32 block-table entries.
+ * Returns 0 for an invalid descriptor or sizes.
+ */
+size_t pkv_prefill_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
+                                       const pkv_cache_desc *d);
+
+/*
+ * pkv_paged_attn_prefill_fp8 -- the prefill over an FP8 E4M3 cache (the
+ * MiMo model card's production setting, "What the kernels do": FP8 K/V,
+ * with Q.K^T kept in 16-bit; its FP8 Q.K^T had 7x the error).  Two passes on
+ * `stream`:
+ *   1. every page a sequence uses (block_table[b][j], j < ceil(seq_lens[b] /
+ *      block_size)) is copied into the workspace as its E4M3 codes widened
+ *      to bf16 (exact), with a remapped block table;
+ *   2. the tcgen05 prefill of pkv_paged_attn_prefill runs on those pages,
+ *      with k_scale folded into the softmax scale and v_scale into the
+ *      output, per KV head (SCALE_HEAD) or per tensor.
+ * Q.K^T is exact products of bf16 q and E4M3 codes summed in f32.  The
+ * result is out = softmax(scale * q (k_scale K)^T) (v_scale V) as in
+ * pkv_paged_attn_prefill, with the attention sink of
+ * pkv_paged_attn_prefill_sink when sinks is not NULL.
+ * cache: FP8 E4M3 (d->dtype PKV_FP8_E4M3); k_scale / v_scale as in the
+ * decode (positive).  workspace: device memory of at least
+ * pkv_prefill_fp8_workspace_bytes(num_seqs, max_blocks_per_seq, d) bytes,
+ * 256-byte aligned, overwritten by the call; overlapping calls must not
+ * share it.  An out-of-range page id is skipped (read as zeros) and
+ * recorded as PKV_EDEV_RANGE.  Status codes as in pkv_paged_attn_prefill;
+ * PKV_EINVAL also for a non-FP8 cache or a missing, misaligned or too small
+ * workspace.
+ */
+int pkv_paged_attn_prefill_fp8(const void *q, int num_q_heads, int num_tokens,
+                               const void *cache, const pkv_cache_desc *d,
+                               const int32_t *block_table, int max_blocks_per_seq,
+                               const int32_t *seq_lens,
+                               const int32_t *query_start_loc, int num_seqs,
+                               float softmax_scale, const float *k_scale,
+                               const float *v_scale, const float *sinks,
+                               void *workspace, size_t workspace_bytes, void *out,
+                               pkv_stream_t stream);
+
+/*
  * pkv_paged_attn_prefill_sink -- pkv_paged_attn_prefill with an attention
  * sink: one extra logit per query head in every row's softmax denominator,
  * with no value vector (MiMo model card, "Update 2026-10-01": the vision
@@ -346,9 +390,10 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /*
  * pkv_supports -- whether this build serves a K/V head-size pair for a cache
- * dtype in each call: bit 0 write, bit 1 prefill, bit 2 decode.  Mirrors the
- * per-backend capability check of vLLM PR #64064 ("Details": v <= k is what
- * a page split at head_size can serve); 0 when v > k.
+ * dtype in each call: bit 0 write, bit 1 prefill (pkv_paged_attn_prefill for
+ * bf16 caches, pkv_paged_attn_prefill_fp8 for FP8 ones), bit 2 decode.
+ * Mirrors the per-backend capability check of vLLM PR #64064 ("Details":
+ * v <= k is what a page split at head_size can serve); 0 when v > k.
  */
 int pkv_supports(int head_size, int head_size_v, int dtype);
 

@@ -35,7 +35,8 @@ EXPORTED = (
     "pkv_kv_cache_write", "pkv_paged_attn_prefill", "pkv_paged_attn_decode",
     "pkv_paged_attn_decode_fused", "pkv_paged_attn_decode_fused_noalloc",
     "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_splitkv_reduce_sink",
-    "pkv_paged_attn_prefill_sink", "pkv_decode_suggest_splits",
+    "pkv_paged_attn_prefill_sink", "pkv_prefill_fp8_workspace_bytes",
+    "pkv_paged_attn_prefill_fp8", "pkv_decode_suggest_splits",
     "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
@@ -105,6 +106,10 @@ def _lib():
         lib.pkv_splitkv_reduce_sink.argtypes = [P, P, I, I, I, P, I, P, P, P]
         lib.pkv_paged_attn_prefill_sink.argtypes = [P, I, I, P, D, P, I, P, P, I,
                                                     F, P, P, P, P, P]
+        lib.pkv_prefill_fp8_workspace_bytes.argtypes = [I, I, D]
+        lib.pkv_prefill_fp8_workspace_bytes.restype = ctypes.c_size_t
+        lib.pkv_paged_attn_prefill_fp8.argtypes = [P, I, I, P, D, P, I, P, P, I, F, P, P,
+                                                   P, P, ctypes.c_size_t, P, P]
         lib.pkv_decode_suggest_splits.argtypes = [I, I, I, I, I, I]
         lib.pkv_supports.argtypes = [I, I, I]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
@@ -113,7 +118,8 @@ def _lib():
         lib.pkv_status_string.argtypes = [I]
         lib.pkv_status_string.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("pkv_status_string", "pkv_decode_workspace_bytes"):
+            if name not in ("pkv_status_string", "pkv_decode_workspace_bytes",
+                            "pkv_prefill_fp8_workspace_bytes"):
                 getattr(lib, name).restype = ctypes.c_int
         _handle = lib
         return lib
@@ -183,12 +189,20 @@ def _attn_common(q, block_table, seq_lens, query_start_loc):
     assert block_table.dim() == 2
 
 
+def prefill_fp8_workspace_bytes(num_seqs, max_blocks_per_seq, cache: Cache) -> int:
+    return int(_lib().pkv_prefill_fp8_workspace_bytes(int(num_seqs), int(max_blocks_per_seq),
+                                                      ctypes.byref(cache.desc)))
+
+
 def paged_attn_prefill(q, cache: Cache, block_table, seq_lens,
                        query_start_loc, softmax_scale, out=None,
-                       k_scale=None, v_scale=None, stream=None, sinks=None):
+                       k_scale=None, v_scale=None, stream=None, sinks=None,
+                       workspace=None):
     """q: bf16 [T, Hq, dk]; returns out bf16 [T, Hq, dv].  ``sinks``: float32
     [Hq] CUDA tensor of attention-sink logits (pkv_paged_attn_prefill_sink),
-    or None."""
+    or None.  An FP8 cache goes through pkv_paged_attn_prefill_fp8 with
+    ``workspace`` (a uint8 CUDA tensor of at least
+    prefill_fp8_workspace_bytes(...) bytes; one is allocated when None)."""
     _attn_common(q, block_table, seq_lens, query_start_loc)
     T, Hq, _ = q.shape
     if out is None:
@@ -198,12 +212,21 @@ def paged_attn_prefill(q, cache: Cache, block_table, seq_lens,
             _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
             _ptr(query_start_loc), int(seq_lens.shape[0]), float(softmax_scale),
             _ptr(k_scale), _ptr(v_scale))
-    if sinks is None:
+    if sinks is not None:
+        assert sinks.dtype == torch.float32 and sinks.is_contiguous()
+        assert tuple(sinks.shape) == (Hq,)
+    if cache.desc.dtype == FP8_E4M3:
+        n = prefill_fp8_workspace_bytes(int(seq_lens.shape[0]), int(block_table.shape[1]),
+                                        cache)
+        if workspace is None:
+            workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        nb = workspace.numel() * workspace.element_size()
+        _check("pkv_paged_attn_prefill_fp8", _lib().pkv_paged_attn_prefill_fp8(
+            *args, _ptr(sinks), _ptr(workspace), nb, _ptr(out), _stream(stream)))
+    elif sinks is None:
         _check("pkv_paged_attn_prefill", _lib().pkv_paged_attn_prefill(
             *args, _ptr(out), _stream(stream)))
     else:
-        assert sinks.dtype == torch.float32 and sinks.is_contiguous()
-        assert tuple(sinks.shape) == (Hq,)
         _check("pkv_paged_attn_prefill_sink", _lib().pkv_paged_attn_prefill_sink(
             *args, _ptr(sinks), _ptr(out), _stream(stream)))
     return out

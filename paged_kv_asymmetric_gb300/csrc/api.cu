@@ -201,7 +201,7 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
                  int max_blocks_per_seq, const int32_t* seq_lens,
                  const int32_t* query_start_loc, int num_seqs, float softmax_scale,
                  const float* k_scale, const float* v_scale, const float* sinks,
-                 void* out, pkv_stream_t stream) {
+                 void* out, pkv_stream_t stream, int fold_scale_mode = -1) {
   int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
                              max_blocks_per_seq, seq_lens, query_start_loc,
                              num_seqs, softmax_scale, k_scale, v_scale);
@@ -229,6 +229,12 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
                                   k_scale, v_scale, err);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.sinks = sinks;
+  if (fold_scale_mode >= 0) {  // FP8 codes widened to bf16: the scales fold in
+    p.fold_scales = 1;
+    p.scale_mode = fold_scale_mode;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+  }
   cudaError_t e = pkv::launch_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
@@ -247,6 +253,80 @@ int pkv_paged_attn_prefill(const void* q, int num_q_heads, int num_tokens,
   return prefill_impl(q, num_q_heads, num_tokens, cache, d, block_table, max_blocks_per_seq,
                       seq_lens, query_start_loc, num_seqs, softmax_scale, k_scale, v_scale,
                       nullptr, out, stream);
+}
+
+namespace {
+
+// The FP8 prefill's workspace: widened pages, then the remapped block table.
+size_t fp8_pages_bytes(int num_seqs, int max_blocks_per_seq, const pkv_cache_desc* d) {
+  const size_t page = static_cast<size_t>(d->block_size) * d->num_kv_heads * d->row_elems * 2;
+  const size_t bytes = static_cast<size_t>(num_seqs) * max_blocks_per_seq * page;
+  return (bytes + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+
+size_t pkv_prefill_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
+                                       const pkv_cache_desc* d) {
+  if (d == nullptr || check_desc(d) != PKV_OK || num_seqs < 0 || max_blocks_per_seq < 1)
+    return 0;
+  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > (int64_t{1} << 31) - 1) return 0;
+  return fp8_pages_bytes(num_seqs, max_blocks_per_seq, d) +
+         static_cast<size_t>(num_seqs) * max_blocks_per_seq * sizeof(int32_t);
+}
+
+int pkv_paged_attn_prefill_fp8(const void* q, int num_q_heads, int num_tokens,
+                               const void* cache, const pkv_cache_desc* d,
+                               const int32_t* block_table, int max_blocks_per_seq,
+                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                               int num_seqs, float softmax_scale, const float* k_scale,
+                               const float* v_scale, const float* sinks, void* workspace,
+                               size_t workspace_bytes, void* out, pkv_stream_t stream) {
+  if (d == nullptr) return PKV_EINVAL;
+  int rc = check_attn_common(q, num_q_heads, num_tokens, cache, d, block_table,
+                             max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                             softmax_scale, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (d->dtype != PKV_FP8_E4M3) return PKV_EINVAL;
+  const size_t need = pkv_prefill_fp8_workspace_bytes(num_seqs, max_blocks_per_seq, d);
+  if (need == 0 && num_seqs > 0) return PKV_EINVAL;
+  if (num_tokens > 0 && (workspace == nullptr || workspace_bytes < need ||
+                         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return PKV_EINVAL;
+  // the widened pages are an ordinary bf16 cache of num_seqs x max_blocks
+  // pages (unscaled codes: the scales fold into the prefill)
+  pkv_cache_desc wd = *d;
+  wd.dtype = PKV_BF16;
+  wd.scale_mode = PKV_SCALE_NONE;
+  wd.num_blocks = num_seqs * max_blocks_per_seq;
+  if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
+  if (wd.num_blocks < 1) return PKV_EINVAL;
+  // every later check of the prefill, on the widened cache, before any launch
+  if (!(softmax_scale > 0.f) || out == nullptr) return PKV_EINVAL;
+  if (!pkv::prefill_supported(wd.head_size, wd.head_size_v, wd.dtype)) return PKV_EUNSUPPORTED;
+  const int G = num_q_heads / d->num_kv_heads;
+  if (128 % G != 0) return PKV_EUNSUPPORTED;
+  const int bs = d->block_size;
+  if (bs < 8 || (bs & (bs - 1)) != 0) return PKV_EUNSUPPORTED;
+  if (!aligned16(cache) || !aligned16(q) || (d->row_elems * 2) % 16 != 0 ||
+      d->k_off % 64 != 0 || d->v_off % 8 != 0)
+    return PKV_EUNSUPPORTED;
+  int* err = nullptr;
+  int sms = 0;
+  rc = device_info(&err, &sms);
+  if (rc != PKV_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto* pages = reinterpret_cast<__nv_bfloat16*>(ws);
+  auto* remap = reinterpret_cast<int32_t*>(ws + fp8_pages_bytes(num_seqs, max_blocks_per_seq, d));
+  const int64_t page_elems = static_cast<int64_t>(bs) * d->num_kv_heads * d->row_elems;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_fp8_pages_to_bf16(
+      static_cast<const uint8_t*>(cache), page_elems, d->num_blocks, block_table,
+      max_blocks_per_seq, seq_lens, num_seqs, bs, pages, remap, err, sms, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return prefill_impl(q, num_q_heads, num_tokens, pages, &wd, remap, max_blocks_per_seq,
+                      seq_lens, query_start_loc, num_seqs, softmax_scale, k_scale, v_scale,
+                      sinks, out, stream, /*fold_scale_mode=*/d->scale_mode);
 }
 
 int pkv_paged_attn_prefill_sink(const void* q, int num_q_heads, int num_tokens,
@@ -553,7 +633,9 @@ int pkv_supports(int head_size, int head_size_v, int dtype) {
   if (head_size < 1 || head_size_v < 1 || head_size_v > head_size) return 0;
   if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return 0;
   int bits = 1;  // the write takes any K / V sizes
-  if (pkv::prefill_supported(head_size, head_size_v, dtype)) bits |= 2;
+  // prefill: pkv_paged_attn_prefill for bf16 caches, pkv_paged_attn_prefill_fp8
+  // (the same kernel on the widened codes) for FP8 ones
+  if (pkv::prefill_supported(head_size, head_size_v, PKV_BF16)) bits |= 2;
   if (pkv::decode_supported(head_size, head_size_v, dtype)) bits |= 4;
   return bits;
 }

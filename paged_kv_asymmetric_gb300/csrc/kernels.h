@@ -59,7 +59,23 @@ struct AttnParams {
   // prefill: one attention-sink logit per query head (nullable), an extra
   // term exp(sink) in each row's softmax denominator
   const float* sinks;
+  // prefill: the cache holds FP8 codes widened to bf16 (the FP8 prefill's
+  // workspace); k_scale is folded into the softmax scale and v_scale into
+  // the output, per KV head (or per tensor)
+  int fold_scales;
 };
+
+// The FP8 prefill's first pass: every page a sequence uses is copied from
+// the FP8 cache into `pages` (bf16, the same page geometry) as its E4M3
+// codes widened exactly to bf16, page j of sequence b to page
+// b * max_blocks_per_seq + j, whose index goes to remap[b][j] (-1 for
+// entries past the sequence's pages).  An out-of-range page id is recorded
+// in err and its remap entry set to -1.
+cudaError_t launch_fp8_pages_to_bf16(const uint8_t* cache, int64_t page_elems, int num_blocks,
+                                     const int32_t* block_table, int max_blocks_per_seq,
+                                     const int32_t* seq_lens, int num_seqs, int block_size,
+                                     __nv_bfloat16* pages, int32_t* remap, int* err,
+                                     int num_sms, cudaStream_t stream);
 
 // The fused decode merges in-kernel up to this many splits (its per-row
 // weights live in shared memory); beyond, the merge is a second launch.

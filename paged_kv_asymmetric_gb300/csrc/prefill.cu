@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = (threadIdx.x - 128) & 127;       // its row of the tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_off + tm_s(x), to = tmem + lane_off + tm_o(x);
-    const float scale_log2 = p.softmax_scale * kLog2e;
+    const float scale_log2_base = p.softmax_scale * kLog2e;
     uint32_t sc = 0;  // S tiles seen
     uint32_t items = 0, fbase = 0;
     // waits whose outcome is the same for the whole warp, so that the warp
@@ -410,6 +410,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int k = 0;; ++k) {
       Item it;
       if (!get_unit(p, TQ, unit_index(k), rank, it)) break;
+      // FP8 caches (their codes widened to bf16): k_scale joins the softmax
+      // scale and v_scale the output, for this item's KV head
+      float scale_log2 = scale_log2_base, v_mul = 1.f;
+      if (p.fold_scales) {
+        const int si = p.scale_mode == PKV_SCALE_HEAD ? it.g : 0;
+        scale_log2 *= __ldg(p.k_scale + si);
+        v_mul = __ldg(p.v_scale + si);
+      }
       const int tr = r / G, hr = r % G;
       const bool valid = tr < it.nq[x];
       const int pos = it.minpos[x] + tr;
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float sk = __ldg(p.sinks + it.g * G + hr);
         if (sk != -INFINITY) l += fast_exp2(fmaf(sk, kLog2e, -m));
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? v_mul / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_supports_mirrors_v_le_k(lib):
     assert pkv.supports(192, 128) == 7
-    assert pkv.supports(192, 128, pkv.FP8_E4M3) == 5   # no fp8 prefill yet
+    assert pkv.supports(192, 128, pkv.FP8_E4M3) == 7   # fp8 prefill: pkv_paged_attn_prefill_fp8
     assert pkv.supports(576, 512) == 5
     assert pkv.supports(128, 192) == 0                  # V wider than K
     assert pkv.supports(64, 64) == 1                    # write only

@@ -1,0 +1,100 @@
+"""The prefill over an FP8 E4M3 cache (pkv_paged_attn_prefill_fp8: the
+batch's pages widened to bf16 codes in a workspace, then the tcgen05
+prefill with the scales folded in) against the oracle, which reads the
+same cache through its own E4M3 decoder.  FP8-KV tolerance: atol 3e-2.
+Unwritten cache bytes hold NaN codes, so the partly filled last page of a
+sequence exercises the tail masking through the widened copy."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_asymmetric_gb300 as pkv
+from paged_kv_asymmetric_gb300 import workloads as wl
+from tests import gpu_path, refs
+
+pytestmark = pytest.mark.gpu
+
+H, T_ = wl.SCALE_HEAD, wl.SCALE_TENSOR
+CASES = {
+    "tiny-head": lambda: wl.tiny("prefill", kv_dtype=wl.FP8, scale_mode=H),
+    "tiny-hnd-tensor": lambda: wl.tiny("prefill", layout=wl.HND, kv_dtype=wl.FP8,
+                                       scale_mode=T_),
+    "ragged-varlen": lambda: wl.make_workload(
+        "rag8", seq_lens=[1, 33, 129, 300], q_lens=[1, 33, 129, 300],
+        kv_dtype=wl.FP8, scale_mode=H, seed=61),
+    "chunked-with-context-b64": lambda: wl.make_workload(
+        "chunk8", seq_lens=[700, 95, 260], q_lens=[150, 31, 1], block_size=64,
+        kv_dtype=wl.FP8, scale_mode=H, seed=62),
+    "block8-hnd": lambda: wl.make_workload(
+        "b8f", seq_lens=[150], q_lens=[150], block_size=8, layout=wl.HND,
+        kv_dtype=wl.FP8, scale_mode=T_, seed=63),
+    "gqa-8": lambda: wl.make_workload(
+        "g8f", seq_lens=[200], q_lens=[200], num_q_heads=16, num_kv_heads=2,
+        kv_dtype=wl.FP8, scale_mode=H, seed=64),
+}
+
+
+def _run(w, tokens=None, seqs=None, sinks=None):
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    gpu_path.device_error()
+    st = None if sinks is None else torch.from_numpy(sinks).cuda()
+    out = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                                 dw.query_start_loc, w.softmax_scale,
+                                 k_scale=dw.k_scale, v_scale=dw.v_scale, sinks=st)
+    torch.cuda.synchronize()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+    o, _ = gpu_path.oracle_rows(w, tokens=tokens, seqs=seqs, sinks=sinks)
+    got = gpu_path.host(out)
+    if tokens is not None:
+        got = got[tokens]
+    refs.assert_close(got, o, **gpu_path.FP8_TOL, what=w.name)
+    return dw, out
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fp8_prefill_small(name):
+    _run(CASES[name]())
+
+
+def test_fp8_prefill_with_sinks():
+    w = CASES["chunked-with-context-b64"]()
+    sinks = np.linspace(-3, 3, w.num_q_heads).astype(np.float32)
+    _run(w, sinks=sinks)
+
+
+def test_fp8_prefill_repeatable_and_workspace_checks():
+    w = CASES["ragged-varlen"]()
+    dw, a = _run(w)
+    b = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                               dw.query_start_loc, w.softmax_scale,
+                               k_scale=dw.k_scale, v_scale=dw.v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    n = pkv.prefill_fp8_workspace_bytes(w.num_seqs, dw.block_table.shape[1], dw.cache)
+    assert n > 0
+    small = torch.empty(n - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                               dw.query_start_loc, w.softmax_scale,
+                               k_scale=dw.k_scale, v_scale=dw.v_scale, workspace=small)
+    assert e.value.status == pkv.EINVAL
+    big = torch.empty(n + 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:  # not 256-byte aligned
+        pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                               dw.query_start_loc, w.softmax_scale,
+                               k_scale=dw.k_scale, v_scale=dw.v_scale, workspace=big[16:])
+    assert e.value.status == pkv.EINVAL
+
+
+def test_fp8_prefill_32k_sampled():
+    """32,768 tokens, FP8 cache with per-head scales, in the bench's launch
+    shape; sampled rows, every head, against the oracle."""
+    w = wl.make_workload("prefill-32768-fp8", seq_lens=[32768], q_lens=[32768],
+                         kv_dtype=wl.FP8, scale_mode=H, seed=0)
+    rng = np.random.default_rng(1)
+    toks = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 32767],
+                                     rng.integers(0, 32768, 8)])).astype(np.int32)
+    _run(w, tokens=toks, seqs=[0])
