@@ -159,6 +159,8 @@ struct DecodeCfg {
   static constexpr int TCS_BYTES = TC ? (2 * 16 + 4 * 16 + 16 + 4) * 4 : 0;
   static constexpr int SMEM = TCS_OFF + TCS_BYTES + 1024;
   static_assert(DK % 64 == 0, "K in 64-column units");
+  // (also reads the warp-MMA form's sizes, which the other forms leave unused)
+  static_assert(NU >= 1 && UPW >= 1 && NT >= 1, "warp-MMA form sizes");
   static_assert(DV % WG == 0 && DVS % (FP8 ? 128 : 16) == 0, "V slices");
   static_assert(QCH % 8 == 0, "Q rows in whole 128-byte groups");
   static_assert(KPC % 16 == 0 && KPC <= 256, "keys per chunk");
