@@ -134,6 +134,54 @@ def test_reduce_rejects_bad_arguments(lib):
     assert f(DUMMY, DUMMY, 2, 0, 128, None, None, None) == pkv.OK
 
 
+def test_reduce_sink_rejects_bad_arguments(lib):
+    f = lib.pkv_splitkv_reduce_sink
+    # rows (6) not a multiple of the query heads (4); no query heads
+    assert f(DUMMY, DUMMY, 2, 6, 128, DUMMY, 4, DUMMY, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 8, 128, DUMMY, 0, DUMMY, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, -1, 8, 128, DUMMY, 4, DUMMY, None, None) == pkv.EINVAL
+    assert f(None, DUMMY, 2, 8, 128, DUMMY, 4, DUMMY, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 8, 128, DUMMY, 4, None, None, None) == pkv.EINVAL
+    assert f(DUMMY, DUMMY, 2, 0, 128, DUMMY, 4, None, None, None) == pkv.OK
+
+
+def test_prefill_fp8_workspace_size(lib):
+    d8 = _desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)   # block 16, 4 heads, row 320
+    f = lib.pkv_prefill_fp8_workspace_bytes
+    f.restype = ctypes.c_size_t
+    page = 16 * 4 * 320 * 2
+    n = f(3, 5, ctypes.byref(d8))
+    pages = (3 * 5 * page + 255) // 256 * 256
+    assert n == pages + 3 * 5 * 4       # widened pages, then the remapped table
+    assert f(3, 0, ctypes.byref(d8)) == 0
+    assert f(-1, 5, ctypes.byref(d8)) == 0
+    assert f(3, 5, None) == 0
+
+
+def test_prefill_fp8_rejects_bad_arguments(lib):
+    d8 = _desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)
+    f = lib.pkv_prefill_fp8_workspace_bytes
+    f.restype = ctypes.c_size_t
+    need = f(1, 4, ctypes.byref(d8))
+    WS = ctypes.c_void_p(1 << 20)       # 256-byte aligned, never dereferenced
+
+    def call(d, ws=WS, nbytes=need, ks=DUMMY, vs=DUMMY, **kw):
+        a = dict(q=DUMMY, Hq=16, T=4, scale=0.1, out=DUMMY)
+        a.update(kw)
+        return lib.pkv_paged_attn_prefill_fp8(
+            a["q"], a["Hq"], a["T"], DUMMY, ctypes.byref(d), DUMMY, 4, DUMMY,
+            DUMMY, 1, ctypes.c_float(a["scale"]), ks, vs, None, ws,
+            ctypes.c_size_t(nbytes), a["out"], None)
+    assert call(_desc()) == pkv.EINVAL                       # a bf16 cache
+    assert call(d8, ks=None) == pkv.EINVAL                   # scales missing
+    assert call(d8, ws=None) == pkv.EINVAL                   # no workspace
+    assert call(d8, nbytes=need - 1) == pkv.EINVAL           # too small
+    assert call(d8, ws=ctypes.c_void_p((1 << 20) + 16)) == pkv.EINVAL  # misaligned
+    assert call(d8, scale=-1.0) == pkv.EINVAL
+    assert call(d8, out=None) == pkv.EINVAL
+    assert call(d8, T=0) == pkv.OK                           # nothing to do
+
+
 def test_status_strings(lib):
     for s in (pkv.OK, pkv.EINVAL, pkv.EUNSUPPORTED, pkv.ECUDA):
         assert lib.pkv_status_string(s)
