@@ -372,13 +372,15 @@ def gpu_arm(args, ws, rank, local):
         elif args.only == "prefill_fp8":
             prefill_fp8_sub(f"prefill_fp8_{args.prefill_tokens}", args.prefill_tokens)
         elif args.only == "verify":
-            attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), 16, time_write=True)
+            attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), args.splits or 16,
+                            time_write=True)
         elif args.only == "mla":
             s = pkv.decode_suggest_splits(1, 16, 1, 1, 100000, 64)
             attn_decode_sub("mla_b1_h16", wl.mla_decode(batch=1, heads=16,
-                                                        device=dev), s)
+                                                        device=dev), args.splits or s)
         elif args.only == "decode":
-            attn_decode_sub("batched_decode", wl.batched_decode(device=dev), 16)
+            wd = wl.batched_decode(device=dev)
+            attn_decode_sub("batched_decode", wd, args.splits or wd.max_splits)
         return {"only": args.only, "sub": sub, "clocks": sampler.stop()}
 
     # ---------------- headline: batched decode step -------------------
@@ -645,6 +647,9 @@ def main(argv=None):
     ap.add_argument("--only", choices=["prefill", "prefill_fp8", "verify", "mla", "decode"],
                     help="run one sub-measurement alone (for profiling)")
     ap.add_argument("--prefill-tokens", type=int, default=8192)
+    ap.add_argument("--splits", type=int, default=0,
+                    help="split-KV segments for --only decode / verify / mla "
+                         "(default: the workload's own count)")
     ap.add_argument("--sub-reps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=30.0)

@@ -7,10 +7,15 @@
 // denominator, vLLM #58235) joins the merge once per row as one more segment
 // with lse = sink and no value: it enters the maximum and the weight sum.
 //
-// One warp per row: the split weights are recomputed by every lane from the
-// (broadcast) lse values, and each lane accumulates four consecutive output
-// columns per pass with 16-byte loads.  The kernel reads S * dv * 4 bytes per
-// row and writes dv * 2; it is small next to the decode it follows.
+// Three forms.  The merge reads S * dv * 4 bytes per row and writes dv * 2,
+// a few MB next to the decode it follows, so its time is memory latency and
+// the number of dependent round trips, not bandwidth:
+//  * up to 32 splits (dv % 4 == 0): one warp per (row, 128 columns); lane s
+//    loads lse_s while every lane already has all S of its 16-byte partial
+//    loads in flight, so a row costs one round trip to memory;
+//  * more splits: a CTA per (row, column block), the splits spread over
+//    its threads;
+//  * dv % 4 != 0: one warp per row, one column per lane.
 #include <math.h>
 
 #include "common.cuh"
@@ -20,6 +25,7 @@ namespace pkv {
 
 namespace {
 
+// dv % 4 != 0 (any split count): one warp per row, one column per lane.
 __global__ void __launch_bounds__(256)
     splitkv_reduce_kernel(const float* __restrict__ po,
                           const float* __restrict__ plse, int S, int rows,
@@ -28,7 +34,6 @@ __global__ void __launch_bounds__(256)
                           int hq) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const bool vec = (dv & 3) == 0;
   for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows;
        r += gridDim.x * wpb) {
     float M = -INFINITY;
@@ -49,48 +54,17 @@ __global__ void __launch_bounds__(256)
     // the sink's weight (0 without a sink)
     const float wsink = sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2));
     float W = 0.f;
-    if (vec) {
-      for (int c0 = 0; c0 < dv; c0 += 128) {
-        const int c = c0 + 4 * lane;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float wsum = wsink;
-        for (int s = 0; s < S; ++s) {
-          const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
-          if (x == -INFINITY) continue;  // empty segment: o_s is not read
-          const float w = fast_exp2(fmaf(x, kLog2e, -Ml2));
-          wsum += w;
-          if (c < dv) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(
-                po + (static_cast<int64_t>(s) * rows + r) * dv + c));
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
-          }
-        }
-        W = wsum;
-        if (c < dv) {
-          const float inv = 1.f / wsum;
-          uint2 st;
-          st.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-          st.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(orow + c) = st;
-        }
+    for (int c = lane; c < dv; c += 32) {
+      float acc = 0.f, wsum = wsink;
+      for (int s = 0; s < S; ++s) {
+        const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
+        if (x == -INFINITY) continue;  // empty segment: o_s is not read
+        const float w = fast_exp2(fmaf(x, kLog2e, -Ml2));
+        wsum += w;
+        acc = fmaf(w, __ldg(po + (static_cast<int64_t>(s) * rows + r) * dv + c), acc);
       }
-    } else {
-      for (int c = lane; c < dv; c += 32) {
-        float acc = 0.f, wsum = wsink;
-        for (int s = 0; s < S; ++s) {
-          const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
-          if (x == -INFINITY) continue;
-          const float w = fast_exp2(fmaf(x, kLog2e, -Ml2));
-          wsum += w;
-          acc = fmaf(w, __ldg(po + (static_cast<int64_t>(s) * rows + r) * dv + c),
-                     acc);
-        }
-        W = wsum;
-        orow[c] = __float2bfloat16_rn(acc / wsum);
-      }
+      W = wsum;
+      orow[c] = __float2bfloat16_rn(acc / wsum);
     }
     if (lse_out != nullptr && lane == 0) {
       lse_out[r] = M + fast_log2(W) * kLn2;
@@ -98,7 +72,75 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One CTA per (row, block of columns) for dv % 4 == 0: the split maxima and
+// Up to SB splits, dv % 4 == 0: warp g of the grid merges columns
+// [128 * cb, 128 * cb + 128) of row g / ncb (cb = g % ncb).  Every partial
+// of the row is loaded before its weight is known; a segment with weight 0
+// (lse -inf, or a weight that underflows) is skipped by a select, so an
+// unwritten partial never reaches the sum.  The weights pass from lane s to
+// the others through shared memory.
+template <int SB>
+__global__ void __launch_bounds__(128)
+    splitkv_reduce_warp4_kernel(const float* __restrict__ po,
+                                const float* __restrict__ plse, int S, int rows,
+                                int dv, __nv_bfloat16* __restrict__ out,
+                                float* __restrict__ lse_out,
+                                const float* __restrict__ sinks, int hq) {
+  static_assert(SB >= 1 && SB <= 32, "one split per lane");
+  __shared__ float wsh[4][SB];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int dv4 = dv >> 2;
+  const int ncb = (dv4 + 31) >> 5;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * 4 + wid;
+  if (g >= static_cast<int64_t>(rows) * ncb) return;  // whole warps; no CTA barrier below
+  const int r = static_cast<int>(g / ncb);
+  const int c4 = static_cast<int>(g - static_cast<int64_t>(r) * ncb) * 32 + lane;
+  const bool in = c4 < dv4;
+  const float x = lane < S ? __ldg(plse + static_cast<int64_t>(lane) * rows + r) : -INFINITY;
+  const float4* po4 = reinterpret_cast<const float4*>(po);
+  float4 v[SB];
+#pragma unroll
+  for (int s = 0; s < SB; ++s)
+    v[s] = (s < S && in) ? __ldg(po4 + (static_cast<int64_t>(s) * rows + r) * dv4 + c4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float sink = sinks != nullptr ? __ldg(sinks + r % hq) : -INFINITY;
+  M = fmaxf(M, sink);
+  __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
+  const bool first = c4 == lane;  // column block 0 writes the row's lse
+  if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
+    if (in) *reinterpret_cast<uint2*>(orow + 4 * c4) = make_uint2(0u, 0u);
+    if (lse_out != nullptr && first && lane == 0) lse_out[r] = -INFINITY;
+    return;
+  }
+  const float Ml2 = M * kLog2e;
+  const float w = x == -INFINITY ? 0.f : fast_exp2(fmaf(x, kLog2e, -Ml2));
+  float W = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  W += sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2));
+  if (lane < SB) wsh[wid][lane] = w;
+  __syncwarp();
+  if (in) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < SB; ++s) {
+      const float ws = wsh[wid][s];
+      const bool use = ws != 0.f;
+      acc.x = use ? fmaf(ws, v[s].x, acc.x) : acc.x;
+      acc.y = use ? fmaf(ws, v[s].y, acc.y) : acc.y;
+      acc.z = use ? fmaf(ws, v[s].z, acc.z) : acc.z;
+      acc.w = use ? fmaf(ws, v[s].w, acc.w) : acc.w;
+    }
+    const float inv = 1.f / W;
+    *reinterpret_cast<uint2*>(orow + 4 * c4) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  }
+  if (lse_out != nullptr && first && lane == 0) lse_out[r] = M + fast_log2(W) * kLn2;
+}
+
+// More than 32 splits, dv % 4 == 0: one CTA per (row, block of columns): the split maxima and
 // weight sums are block reductions (repeated by each column block of a row:
 // S values), and the threads form `ngrp` groups over the splits x `cols`
 // lanes over 16-byte column pieces, so that a row with hundreds of splits is
@@ -215,6 +257,25 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
                                   cudaStream_t stream, const float* sinks,
                                   int num_q_heads) {
   if (num_rows == 0) return cudaSuccess;
+  if ((head_size_v & 3) == 0 && num_splits <= 32) {
+    const int64_t warps = static_cast<int64_t>(num_rows) * ((head_size_v / 4 + 31) / 32);
+    const int64_t blocks = (warps + 3) / 4;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(blocks);
+    if (num_splits <= 8)
+      splitkv_reduce_warp4_kernel<8><<<grid, 128, 0, stream>>>(
+          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
+          num_q_heads);
+    else if (num_splits <= 16)
+      splitkv_reduce_warp4_kernel<16><<<grid, 128, 0, stream>>>(
+          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
+          num_q_heads);
+    else
+      splitkv_reduce_warp4_kernel<32><<<grid, 128, 0, stream>>>(
+          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
+          num_q_heads);
+    return cudaGetLastError();
+  }
   if ((head_size_v & 3) == 0) {
     // column blocks (a power of two dividing dv/4, >= 8 pieces each) until
     // there are about 2 x 152 CTAs

@@ -1,5 +1,9 @@
 """Split-KV merge on the GPU against the oracle, with empty segments and
-rows whose segments are all empty (MiMo model card, "Update 2026-10-01")."""
+rows whose segments are all empty (MiMo model card, "Update 2026-10-01").
+The cases span the merge's three forms: up to 32 splits (one warp per row
+and 128 columns, in its 8-, 16- and 32-split instantiations, dv 512 as four
+column blocks), more than 32 splits (a CTA per row and column block), and
+dv not a multiple of 4 (one warp per row)."""
 from __future__ import annotations
 
 import numpy as np
@@ -13,8 +17,12 @@ from tests import refs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("S,rows,dv", [(1, 7, 128), (16, 300, 128),
-                                       (96, 33, 512), (5, 10, 24), (3, 4, 6)])
+CASES = [(1, 7, 128), (16, 300, 128), (96, 33, 512), (5, 10, 24), (3, 4, 6),
+         (8, 5, 128), (9, 13, 128), (17, 21, 128), (32, 64, 128), (19, 30, 512),
+         (33, 11, 128), (32, 3, 36), (16, 1536, 128), (40, 2, 6)]
+
+
+@pytest.mark.parametrize("S,rows,dv", CASES)
 def test_reduce_matches_oracle(S, rows, dv):
     rng = np.random.default_rng(S * 1000 + rows)
     po = rng.standard_normal((S, rows, dv)).astype(np.float32)
@@ -42,3 +50,35 @@ def test_reduce_zero_splits_gives_zero():
     out = torch.full((4, 128), 7.0, dtype=torch.bfloat16, device="cuda")
     pkv.splitkv_reduce(po, pl, out=out)
     assert (out == 0).all()
+
+
+@pytest.mark.parametrize("S,rows,dv", [(4, 12, 128), (19, 32, 512), (32, 8, 128),
+                                       (48, 8, 128), (6, 8, 10)])
+def test_reduce_with_sinks_matches_oracle(S, rows, dv):
+    """The sink joins each row's merge once (4 query heads: row r takes
+    sink r % 4); head 1's sink is -inf (no sink).  A row with no visible
+    key but a sink has output 0 and lse = the sink."""
+    hq = 4
+    rng = np.random.default_rng(S * 7 + rows)
+    po = rng.standard_normal((S, rows, dv)).astype(np.float32)
+    pl = (rng.standard_normal((S, rows)) * 4).astype(np.float32)
+    pl[rng.random((S, rows)) < 0.3] = -np.inf
+    pl[:, 1] = -np.inf   # no key and no sink (head 1): 0, lse -inf
+    pl[:, 2] = -np.inf   # no key, sink 3.0: 0, lse 3.0
+    po[np.isneginf(pl)] = np.nan
+    sinks = np.array([0.5, -np.inf, 3.0, -2.0], np.float32)
+    ref, rlse = oracle.splitkv_reduce(po, pl, sinks=sinks, num_q_heads=hq)
+    lse = torch.empty(rows, dtype=torch.float32, device="cuda")
+    # rows as [tokens, query heads]: the binding takes Hq from the last axis
+    out = pkv.splitkv_reduce(torch.from_numpy(po.reshape(S, rows // hq, hq, dv)).cuda(),
+                             torch.from_numpy(pl.reshape(S, rows // hq, hq)).cuda(),
+                             lse_out=lse, sinks=torch.from_numpy(sinks).cuda())
+    got = out.reshape(rows, dv).float().cpu().numpy()
+    gl = lse.cpu().numpy()
+    assert np.isfinite(got).all()
+    refs.assert_close(got, ref, atol=1e-2, rtol=1e-2, what="reduce with sinks")
+    fin = np.isfinite(rlse)
+    assert (np.isneginf(gl) == ~fin).all()
+    refs.assert_close(gl[fin], rlse[fin], atol=1e-5, rtol=1e-5)
+    assert (got[1] == 0).all() and np.isneginf(gl[1])
+    assert (got[2] == 0).all() and abs(gl[2] - 3.0) < 1e-5
