@@ -140,13 +140,16 @@ __global__ void __launch_bounds__(128)
   if (lse_out != nullptr && first && lane == 0) lse_out[r] = M + fast_log2(W) * kLn2;
 }
 
-// More than 32 splits, dv % 4 == 0: one CTA per (row, block of columns): the split maxima and
-// weight sums are block reductions (repeated by each column block of a row:
-// S values), and the threads form `ngrp` groups over the splits x `cols`
-// lanes over 16-byte column pieces, so that a row with hundreds of splits is
-// read by hundreds of loads in flight instead of one warp's serial walk.
-// Rows are split into column blocks when there are too few rows to fill the
-// GPU (e.g. one token of an MLA decode with 150+ splits).
+// More than 32 splits, dv % 4 == 0: one CTA per (row, block of columns).
+// The threads form `ngrp` groups over the splits x `cols` lanes over 16-byte
+// column pieces.  Each thread loads its splits' lse values and partials
+// together (eight splits per step, all in flight) and keeps them relative to
+// its own running maximum, rescaling when a later step raises it, as an
+// online softmax does.  The CTA then takes the row maximum (the sink
+// included), rescales each group's sums to it, and adds the groups through
+// shared memory, so a row costs one round trip to memory.  Rows are split
+// into column blocks when there are too few rows to fill the GPU (e.g. one
+// token of an MLA decode with 300 splits).
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
     splitkv_reduce_rows_kernel(const float* __restrict__ po,
@@ -173,79 +176,83 @@ __global__ void __launch_bounds__(THREADS)
     for (int w = 1; w < THREADS / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
     return v;
   };
-  float M = -INFINITY;
-  for (int s = tid; s < S; s += THREADS)
-    M = fmaxf(M, __ldg(plse + static_cast<int64_t>(s) * rows + r));
-  M = block_reduce(M, true);
   const float sink = sinks != nullptr ? __ldg(sinks + r % hq) : -INFINITY;
-  M = fmaxf(M, sink);
   __nv_bfloat16* orow = out + static_cast<int64_t>(r) * dv;
   const int dv4 = dv >> 2;
   const int cb4 = dv4 / ncb;  // 16-byte pieces of this block
   const int c4_lo = blockIdx.y * cb4;
-  if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
-    for (int c = tid; c < 4 * cb4; c += THREADS) orow[4 * c4_lo + c] = __float2bfloat16_rn(0.f);
-    if (lse_out != nullptr && tid == 0 && blockIdx.y == 0) lse_out[r] = -INFINITY;
-    return;
-  }
-  const float Ml2 = M * kLog2e;
-  float wsum = 0.f;
-  for (int s = tid; s < S; s += THREADS) {
-    const float x = __ldg(plse + static_cast<int64_t>(s) * rows + r);
-    if (x != -INFINITY) wsum += fast_exp2(fmaf(x, kLog2e, -Ml2));
-  }
-  const float W = block_reduce(wsum, false) +
-                  (sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2)));
-  const float inv = 1.f / W;
   const int cols = cb4 < THREADS ? cb4 : THREADS;
   const int ngrp = THREADS / cols;
   const int c = tid % cols, grp = tid / cols;
+  const bool grp_ok = grp < ngrp;  // the last THREADS % cols threads idle
+  const float4* po4 = reinterpret_cast<const float4*>(po);
   for (int c0 = 0; c0 < cb4; c0 += cols) {
     const int c4 = c4_lo + c0 + c;
-    const bool in = c0 + c < cb4;
+    const bool in = grp_ok && c0 + c < cb4;
+    // this thread's splits grp, grp + ngrp, ...: weight sum and weighted
+    // partials relative to their running maximum m
+    float m = -INFINITY, ws = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (grp < ngrp && in) {
-      // four splits per step, their loads independent of each other
-      constexpr int U = 4;
-      for (int s0 = grp; s0 < S; s0 += U * ngrp) {
-        float w[U];
-        float4 v[U];
+    constexpr int U = 8;
+    for (int s0 = grp; s0 < S; s0 += U * ngrp) {
+      float x[U];
+      float4 v[U];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int s = s0 + k * ngrp;
-          const float x = s < S ? __ldg(plse + static_cast<int64_t>(s) * rows + r)
-                                : -INFINITY;
-          // an empty segment's o_s is not read
-          w[k] = x == -INFINITY ? 0.f : fast_exp2(fmaf(x, kLog2e, -Ml2));
-          v[k] = w[k] != 0.f
-                     ? __ldg(reinterpret_cast<const float4*>(
-                                 po + (static_cast<int64_t>(s) * rows + r) * dv) + c4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-          acc.x = fmaf(w[k], v[k].x, acc.x);
-          acc.y = fmaf(w[k], v[k].y, acc.y);
-          acc.z = fmaf(w[k], v[k].z, acc.z);
-          acc.w = fmaf(w[k], v[k].w, acc.w);
-        }
+      for (int k = 0; k < U; ++k) {
+        const int s = s0 + k * ngrp;
+        x[k] = (grp_ok && s < S) ? __ldg(plse + static_cast<int64_t>(s) * rows + r) : -INFINITY;
+        v[k] = (in && s < S) ? __ldg(po4 + (static_cast<int64_t>(s) * rows + r) * dv4 + c4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float mb = m;
+#pragma unroll
+      for (int k = 0; k < U; ++k) mb = fmaxf(mb, x[k]);
+      if (mb == -INFINITY) continue;  // no visible segment so far
+      const float mbl2 = mb * kLog2e;
+      const float f = m == -INFINITY ? 0.f : fast_exp2(fmaf(m, kLog2e, -mbl2));
+      ws *= f;
+      acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        // an empty segment (lse -inf) has weight 0 and its partial is skipped
+        const float w = x[k] == -INFINITY ? 0.f : fast_exp2(fmaf(x[k], kLog2e, -mbl2));
+        const bool use = w != 0.f;
+        ws += w;
+        acc.x = use ? fmaf(w, v[k].x, acc.x) : acc.x;
+        acc.y = use ? fmaf(w, v[k].y, acc.y) : acc.y;
+        acc.z = use ? fmaf(w, v[k].z, acc.z) : acc.z;
+        acc.w = use ? fmaf(w, v[k].w, acc.w) : acc.w;
+      }
+      m = mb;
     }
-    __syncthreads();
-    part[tid] = acc;
+    // the row maximum over all groups and the sink (uniform over the CTA)
+    const float M = fmaxf(block_reduce(m, true), sink);
+    if (M == -INFINITY) {  // no segment saw a key: 0, never NaN
+      if (grp == 0 && in) *reinterpret_cast<uint2*>(orow + 4 * c4) = make_uint2(0u, 0u);
+      if (lse_out != nullptr && tid == 0 && blockIdx.y == 0 && c0 == 0) lse_out[r] = -INFINITY;
+      continue;
+    }
+    const float Ml2 = M * kLog2e;
+    const float f = m == -INFINITY ? 0.f : fast_exp2(fmaf(m, kLog2e, -Ml2));
+    acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+    // every lane of a group holds the group's weight sum: count it once
+    const float W = block_reduce(c == 0 && grp_ok ? ws * f : 0.f, false) +
+                    (sink == -INFINITY ? 0.f : fast_exp2(fmaf(sink, kLog2e, -Ml2)));
+    part[tid] = acc;  // block_reduce ended with a barrier after its last write
     __syncthreads();
     if (grp == 0 && in) {
       for (int g2 = 1; g2 < ngrp; ++g2) {
         const float4 v = part[g2 * cols + c];
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
-      uint2 st;
-      st.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      st.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(orow + 4 * c4) = st;
+      const float inv = 1.f / W;
+      *reinterpret_cast<uint2*>(orow + 4 * c4) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     }
+    if (lse_out != nullptr && tid == 0 && blockIdx.y == 0 && c0 == 0)
+      lse_out[r] = M + fast_log2(W) * kLn2;
+    __syncthreads();  // part[] is read before the next pass writes it
   }
-  if (lse_out != nullptr && tid == 0 && blockIdx.y == 0) lse_out[r] = M + fast_log2(W) * kLn2;
 }
 
 }  // namespace

@@ -19,7 +19,10 @@ pytestmark = pytest.mark.gpu
 
 CASES = [(1, 7, 128), (16, 300, 128), (96, 33, 512), (5, 10, 24), (3, 4, 6),
          (8, 5, 128), (9, 13, 128), (17, 21, 128), (32, 64, 128), (19, 30, 512),
-         (33, 11, 128), (32, 3, 36), (16, 1536, 128), (40, 2, 6)]
+         (33, 11, 128), (32, 3, 36), (16, 1536, 128), (40, 2, 6),
+         # > 512 splits: a thread of the CTA-per-row form takes more than one
+         # step of eight splits and rescales to a later, larger maximum
+         (600, 3, 128), (1100, 4, 512), (304, 16, 512)]
 
 
 @pytest.mark.parametrize("S,rows,dv", CASES)
@@ -53,7 +56,7 @@ def test_reduce_zero_splits_gives_zero():
 
 
 @pytest.mark.parametrize("S,rows,dv", [(4, 12, 128), (19, 32, 512), (32, 8, 128),
-                                       (48, 8, 128), (6, 8, 10)])
+                                       (48, 8, 128), (6, 8, 10), (700, 4, 128)])
 def test_reduce_with_sinks_matches_oracle(S, rows, dv):
     """The sink joins each row's merge once (4 query heads: row r takes
     sink r % 4); head 1's sink is -inf (no sink).  A row with no visible
