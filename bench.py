@@ -422,9 +422,14 @@ def gpu_arm(args, ws, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # The decode launches of every 4th step are timed with a pair of events
+    # (the roofline's average launch time).  An event record stands between
+    # two kernels in the stream, where it costs time and keeps the second
+    # from launching before the first ends; the other steps run as a user's
+    # would.
     t0.record(stream)
-    for _ in range(args.steps):
-        step(record=True)
+    for i in range(args.steps):
+        step(record=(i % 4 == 0))
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -442,9 +447,12 @@ def gpu_arm(args, ws, rank, local):
     # ---------------- e2e: host buffers through the public API ---------
     # Every step's inputs (Q, new K/V, slots, block table, seq_lens,
     # query_start_loc) travel host -> device as one copy from a pinned
-    # staging buffer, and its output device -> host, on a copy stream; two
-    # device buffer sets let step k+1's upload and step k's download overlap
-    # step k's kernels.  The timed region ends when the last download lands.
+    # staging buffer on an upload stream, and its output device -> host on a
+    # download stream; two device buffer sets let step k+1's upload and step
+    # k's download overlap step k's kernels (one stream for both directions
+    # would queue each upload behind the previous step's download, which
+    # waits for that step's merge).  The timed region ends when the last
+    # download lands.
     srcs = (dw.q, k_new, v_new, dw.slots_new, dw.block_table, dw.seq_lens,
             dw.query_start_loc)
     offs, off = [], 0
@@ -464,7 +472,8 @@ def gpu_arm(args, ws, rank, local):
     h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in srcs)
     d2h = h_outs[0].numel() * h_outs[0].element_size()
-    cs = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     in_free = [torch.cuda.Event() for _ in range(2)]
     out_ready = [torch.cuda.Event() for _ in range(2)]
@@ -475,10 +484,10 @@ def gpu_arm(args, ws, rank, local):
     def e2e_step(k):
         b = k & 1
         d_q, d_k, d_v, d_slots, d_bt, d_sl, d_qsl = d_views[b]
-        with torch.cuda.stream(cs):
-            cs.wait_event(in_free[b])
+        with torch.cuda.stream(up):
+            up.wait_event(in_free[b])
             d_in[b].copy_(h_in, non_blocking=True)
-            in_ready[b].record(cs)
+            in_ready[b].record(up)
         stream.wait_event(in_ready[b])
         stream.wait_event(out_read[b])
         pkv.kv_cache_write(d_k, d_v, d_slots, dw.cache)
@@ -488,19 +497,20 @@ def gpu_arm(args, ws, rank, local):
         in_free[b].record(stream)
         pkv.splitkv_reduce(po, pl, out=outs[b])
         out_ready[b].record(stream)
-        with torch.cuda.stream(cs):
-            cs.wait_event(out_ready[b])
+        with torch.cuda.stream(down):
+            down.wait_event(out_ready[b])
             h_outs[b].copy_(outs[b], non_blocking=True)
-            out_read[b].record(cs)
+            out_read[b].record(down)
 
     for k in range(3):
         e2e_step(k)
     torch.cuda.synchronize()
     barrier(ws)
     t0.record(stream)
+    up.wait_stream(stream)  # no upload starts before the timed region
     for k in range(args.steps):
         e2e_step(k)
-    stream.wait_stream(cs)
+    stream.wait_stream(down)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)

@@ -59,6 +59,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "tc5.cuh"
 #include "tmap.h"
 
@@ -382,6 +383,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map,
                   const __grid_constant__ CUtensorMap kv_map64, const AttnParams p,
                   int head_boxes) {
+  // the next kernel of the step may start launching; nothing here (TMEM
+  // included) is touched before the kernel ahead has completed
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   constexpr bool FP8 = C::FP8;
   constexpr int HPC = C::HPC, WG = C::WG, NG = C::NG, KPC = C::KPC, NSLOT = C::NSLOT;
@@ -1707,8 +1712,9 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
                         (p.num_kv_heads / C::HPC) * RG;
   const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
   const int grid = static_cast<int>(units < slots ? units : slots);
-  decode_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(kv_map, kv_map64, p, head_boxes);
-  return cudaGetLastError();
+  e = launch_pdl(decode_kernel<C>, grid, C::THREADS, C::SMEM, stream, kv_map, kv_map64, p,
+                 head_boxes);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // <DK, DV, fp8, heads per chunk, warps per group, chunk classes, keys per

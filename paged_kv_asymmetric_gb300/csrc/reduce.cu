@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace pkv {
 
@@ -32,6 +33,8 @@ __global__ void __launch_bounds__(256)
                           int dv, __nv_bfloat16* __restrict__ out,
                           float* __restrict__ lse_out, const float* __restrict__ sinks,
                           int hq) {
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows;
@@ -86,6 +89,8 @@ __global__ void __launch_bounds__(128)
                                 float* __restrict__ lse_out,
                                 const float* __restrict__ sinks, int hq) {
   static_assert(SB >= 1 && SB <= 32, "one split per lane");
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   __shared__ float wsh[4][SB];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int dv4 = dv >> 2;
@@ -158,6 +163,8 @@ __global__ void __launch_bounds__(THREADS)
                                float* __restrict__ lse_out,
                                const float* __restrict__ sinks, int hq) {
   __shared__ float red[THREADS / 32];
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   __shared__ float4 part[THREADS];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int r = blockIdx.x;
@@ -269,19 +276,11 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
     const int64_t blocks = (warps + 3) / 4;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(blocks);
-    if (num_splits <= 8)
-      splitkv_reduce_warp4_kernel<8><<<grid, 128, 0, stream>>>(
-          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
-          num_q_heads);
-    else if (num_splits <= 16)
-      splitkv_reduce_warp4_kernel<16><<<grid, 128, 0, stream>>>(
-          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
-          num_q_heads);
-    else
-      splitkv_reduce_warp4_kernel<32><<<grid, 128, 0, stream>>>(
-          partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
-          num_q_heads);
-    return cudaGetLastError();
+    auto kernel = num_splits <= 8    ? splitkv_reduce_warp4_kernel<8>
+                  : num_splits <= 16 ? splitkv_reduce_warp4_kernel<16>
+                                     : splitkv_reduce_warp4_kernel<32>;
+    return launch_pdl(kernel, grid, 128, 0, stream, partial_o, partial_lse, num_splits,
+                      num_rows, head_size_v, out, lse_out, sinks, num_q_heads);
   }
   if ((head_size_v & 3) == 0) {
     // column blocks (a power of two dividing dv/4, >= 8 pieces each) until
@@ -291,18 +290,15 @@ cudaError_t launch_splitkv_reduce(const float* partial_o,
     while (static_cast<int64_t>(num_rows) * ncb < 304 && dv4 % (2 * ncb) == 0 &&
            dv4 / (2 * ncb) >= 8)
       ncb *= 2;
-    splitkv_reduce_rows_kernel<512><<<dim3(num_rows, ncb), 512, 0, stream>>>(
-        partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
-        num_q_heads);
-    return cudaGetLastError();
+    return launch_pdl(splitkv_reduce_rows_kernel<512>, dim3(num_rows, ncb), 512, 0, stream,
+                      partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out,
+                      sinks, num_q_heads);
   }
   const int wpb = 8;
   int blocks = (num_rows + wpb - 1) / wpb;
   if (blocks > 65535) blocks = 65535;
-  splitkv_reduce_kernel<<<blocks, 32 * wpb, 0, stream>>>(
-      partial_o, partial_lse, num_splits, num_rows, head_size_v, out, lse_out, sinks,
-      num_q_heads);
-  return cudaGetLastError();
+  return launch_pdl(splitkv_reduce_kernel, blocks, 32 * wpb, 0, stream, partial_o, partial_lse,
+                    num_splits, num_rows, head_size_v, out, lse_out, sinks, num_q_heads);
 }
 
 }  // namespace pkv

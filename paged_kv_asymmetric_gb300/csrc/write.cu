@@ -11,6 +11,7 @@
 // (e * (dk + dv)).
 #include "common.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 
 namespace pkv {
 
@@ -77,6 +78,8 @@ __device__ __forceinline__ uint16_t enc2_by(float a, float b, float s, float y) 
 template <bool FP8, int EPT>
 __global__ void __launch_bounds__(256)
     cache_write_vec_kernel(WriteParams p) {
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   constexpr int PPL = 8;                      // pieces per lane per round
   constexpr int NV = EPT / 8;                 // 16-byte source loads per piece
   const int lane = threadIdx.x & 31;
@@ -160,6 +163,8 @@ __global__ void __launch_bounds__(256)
 template <bool FP8, int EPT, int PPL>
 __global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 : 8)) ? 3 : 1)
     cache_write_tok_kernel(WriteParams p) {
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   constexpr int NV = EPT / 8;  // 16-byte source loads per piece
   const int lane = threadIdx.x & 31;
   const int kp = p.head_size / EPT;
@@ -258,6 +263,8 @@ __global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 
 template <bool FP8>
 __global__ void __launch_bounds__(256)
     cache_write_scalar_kernel(WriteParams p, int64_t total_items) {
+  pdl_trigger();  // the next kernel of the step may start launching
+  pdl_wait();     // every global access comes after the kernel ahead completes
   const int per_head = p.head_size + (p.has_value ? p.head_size_v : 0);
   const int64_t nslots = static_cast<int64_t>(p.num_blocks) * p.block_size;
   for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) +
@@ -343,36 +350,37 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
   const int64_t dst_span = static_cast<int64_t>(p.num_kv_heads) * p.block_size * p.row_elems;
   const bool tok = (fp8 ? vec_ok(ept) : vec_ok(8)) && pieces <= 512 &&
                    src_span < (int64_t{1} << 31) && dst_span < (int64_t{1} << 31);
+  cudaError_t e = cudaSuccess;
   if (tok) {
     if (!fp8) {
-      if (pieces <= 128) cache_write_tok_kernel<false, 8, 4><<<tgrid, threads, 0, stream>>>(p);
-      else if (pieces <= 160) cache_write_tok_kernel<false, 8, 5><<<tgrid, threads, 0, stream>>>(p);
-      else if (pieces <= 256) cache_write_tok_kernel<false, 8, 8><<<tgrid, threads, 0, stream>>>(p);
-      else cache_write_tok_kernel<false, 8, 16><<<tgrid, threads, 0, stream>>>(p);
+      if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<false, 8, 4>, tgrid, threads, 0, stream, p);
+      else if (pieces <= 160) e = launch_pdl(cache_write_tok_kernel<false, 8, 5>, tgrid, threads, 0, stream, p);
+      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<false, 8, 8>, tgrid, threads, 0, stream, p);
+      else e = launch_pdl(cache_write_tok_kernel<false, 8, 16>, tgrid, threads, 0, stream, p);
     } else if (ept == 16) {
-      if (pieces <= 96) cache_write_tok_kernel<true, 16, 3><<<tgrid, threads, 0, stream>>>(p);
-      else if (pieces <= 128) cache_write_tok_kernel<true, 16, 4><<<tgrid, threads, 0, stream>>>(p);
-      else if (pieces <= 256) cache_write_tok_kernel<true, 16, 8><<<tgrid, threads, 0, stream>>>(p);
-      else cache_write_tok_kernel<true, 16, 16><<<tgrid, threads, 0, stream>>>(p);
+      if (pieces <= 96) e = launch_pdl(cache_write_tok_kernel<true, 16, 3>, tgrid, threads, 0, stream, p);
+      else if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<true, 16, 4>, tgrid, threads, 0, stream, p);
+      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<true, 16, 8>, tgrid, threads, 0, stream, p);
+      else e = launch_pdl(cache_write_tok_kernel<true, 16, 16>, tgrid, threads, 0, stream, p);
     } else {
-      if (pieces <= 128) cache_write_tok_kernel<true, 8, 4><<<tgrid, threads, 0, stream>>>(p);
-      else if (pieces <= 256) cache_write_tok_kernel<true, 8, 8><<<tgrid, threads, 0, stream>>>(p);
-      else cache_write_tok_kernel<true, 8, 16><<<tgrid, threads, 0, stream>>>(p);
+      if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<true, 8, 4>, tgrid, threads, 0, stream, p);
+      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<true, 8, 8>, tgrid, threads, 0, stream, p);
+      else e = launch_pdl(cache_write_tok_kernel<true, 8, 16>, tgrid, threads, 0, stream, p);
     }
   } else if (!fp8 && vec_ok(8)) {
-    cache_write_vec_kernel<false, 8><<<vgrid, threads, 0, stream>>>(p);
+    e = launch_pdl(cache_write_vec_kernel<false, 8>, vgrid, threads, 0, stream, p);
   } else if (fp8 && vec_ok(16)) {
-    cache_write_vec_kernel<true, 16><<<vgrid, threads, 0, stream>>>(p);
+    e = launch_pdl(cache_write_vec_kernel<true, 16>, vgrid, threads, 0, stream, p);
   } else if (fp8 && vec_ok(8)) {
-    cache_write_vec_kernel<true, 8><<<vgrid, threads, 0, stream>>>(p);
+    e = launch_pdl(cache_write_vec_kernel<true, 8>, vgrid, threads, 0, stream, p);
   } else {
     int64_t items = th * (p.head_size + (p.has_value ? p.head_size_v : 0));
     if (fp8)
-      cache_write_scalar_kernel<true><<<grid_for(items), threads, 0, stream>>>(p, items);
+      e = launch_pdl(cache_write_scalar_kernel<true>, grid_for(items), threads, 0, stream, p, items);
     else
-      cache_write_scalar_kernel<false><<<grid_for(items), threads, 0, stream>>>(p, items);
+      e = launch_pdl(cache_write_scalar_kernel<false>, grid_for(items), threads, 0, stream, p, items);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pkv
