@@ -30,6 +30,17 @@
  *     PKV_E* code.  Arguments are validated on the host before anything is
  *     launched; a rejected call launches nothing.  PKV_ECUDA means a launch
  *     failed; pkv_last_cuda_error() returns the cudaError_t value.
+ *   - Stream order holds as for any kernel launch.  The kernels of
+ *     pkv_kv_cache_write, pkv_paged_attn_decode(_fused, _noalloc) and
+ *     pkv_splitkv_reduce(_sink) use programmatic dependent launch so that
+ *     the next kernel can be placed while the current one finishes.  Each
+ *     waits for everything ahead of it on the stream before it touches
+ *     memory.  A caller's own kernel queued behind one of them sees that
+ *     kernel's results as usual.  The exception is a kernel launched with
+ *     the programmatic-stream-serialization attribute: it must wait
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before reading
+ *     them, as that attribute requires.  PKV_PDL=0 in the environment
+ *     (read once per process) launches them without the attribute.
  *   - bf16 tensors are IEEE bfloat16; fp8 is OCP FP8 E4M3 ("e4m3fn":
  *     saturating, max 448, no infinities).
  *   - Sequences: sequence b has q_len(b) = query_start_loc[b+1] -
