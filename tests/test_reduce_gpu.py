@@ -22,7 +22,10 @@ CASES = [(1, 7, 128), (16, 300, 128), (96, 33, 512), (5, 10, 24), (3, 4, 6),
          (33, 11, 128), (32, 3, 36), (16, 1536, 128), (40, 2, 6),
          # > 512 splits: a thread of the CTA-per-row form takes more than one
          # step of eight splits and rescales to a later, larger maximum
-         (600, 3, 128), (1100, 4, 512), (304, 16, 512)]
+         (600, 3, 128), (1100, 4, 512), (304, 16, 512),
+         # column pieces that do not divide the CTA's 512 threads (the last
+         # threads belong to no group), and a single piece per row
+         (40, 5, 24), (33, 7, 4)]
 
 
 @pytest.mark.parametrize("S,rows,dv", CASES)
