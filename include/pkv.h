@@ -253,7 +253,8 @@ int pkv_paged_attn_prefill_sink(const void *q, int num_q_heads, int num_tokens,
  * K and V are dequantised with k_scale / v_scale for fp8 caches.  Merge the
  * segments with pkv_splitkv_reduce.  partial_o: float32
  * [num_splits][num_tokens][num_q_heads][head_size_v]; partial_lse: float32
- * [num_splits][num_tokens][num_q_heads].  Other arguments as in prefill.
+ * [num_splits][num_tokens][num_q_heads]; both 4-byte aligned (PKV_EINVAL
+ * otherwise).  Other arguments as in prefill.
  * A sequence with seq_lens[b] == 0 (a padded row) gives -inf everywhere; its
  * block-table row is never read.  max_query_len bounds q_len(b) for the
  * launch shape (1 .. 64).
@@ -300,7 +301,9 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads,
  * pkv_paged_attn_decode).  For num_splits > 32 the merge runs as a second
  * launch on the same stream (same results, workspace untouched).  Other
  * arguments, sizes and status codes as in pkv_paged_attn_decode; PKV_EINVAL
- * also for a missing or too small workspace or a null out.
+ * also for a missing or too small workspace, a null out, partial_o not
+ * 16-byte aligned, out not 8-byte aligned, or num_tokens * num_q_heads of
+ * 2^31 or more (the merge reads the partials 16 bytes at a time).
  */
 int pkv_paged_attn_decode_fused(const void *q, int num_q_heads, int num_tokens,
                                 const void *cache, const pkv_cache_desc *d,
@@ -351,13 +354,16 @@ int pkv_paged_attn_decode_fused_noalloc(const void *q, int num_q_heads,
  *
  * For each row r < num_rows: M = max_s partial_lse[s][r].  If M is -inf, or
  * num_splits is 0, out[r][:] = 0 and lse_out[r] = -inf (never NaN).
- * Otherwise w_s = exp(partial_lse[s][r] - M) (segments at -inf are skipped
- * and their partial_o is not read), out[r][:] = sum_s w_s * partial_o[s][r][:]
+ * Otherwise w_s = exp(partial_lse[s][r] - M) (segments at -inf are skipped:
+ * their partial_o values never enter the sum and may be left unwritten, as
+ * the decode leaves them), out[r][:] = sum_s w_s * partial_o[s][r][:]
  * / sum_s w_s, rounded to bf16, and lse_out[r] = M + log(sum_s w_s).
- * partial_o: float32 [num_splits][num_rows][head_size_v]; partial_lse:
- * float32 [num_splits][num_rows]; out: bf16 [num_rows][head_size_v];
- * lse_out: float32 [num_rows] or NULL.  For the decode call, num_rows =
- * num_tokens * num_q_heads.
+ * partial_o: float32 [num_splits][num_rows][head_size_v] (all of it must be
+ * allocated); partial_lse: float32 [num_splits][num_rows]; out: bf16
+ * [num_rows][head_size_v]; lse_out: float32 [num_rows] or NULL.  For the
+ * decode call, num_rows = num_tokens * num_q_heads.  When head_size_v is a
+ * multiple of 4, partial_o must be 16-byte aligned and out 8-byte aligned
+ * (PKV_EINVAL otherwise).
  */
 int pkv_splitkv_reduce(const float *partial_o, const float *partial_lse,
                        int num_splits, int num_rows, int head_size_v,

@@ -361,6 +361,9 @@ int decode_prepare(const void* q, int num_q_heads, int num_tokens, const void* c
   if (num_splits < 1 || num_splits > 65535) return PKV_EINVAL;
   if (num_tokens > 0 && (partial_o == nullptr || partial_lse == nullptr))
     return PKV_EINVAL;
+  if (((reinterpret_cast<uintptr_t>(partial_o) | reinterpret_cast<uintptr_t>(partial_lse)) &
+       3u) != 0)
+    return PKV_EINVAL;  // float stores
   if (!pkv::decode_supported(d->head_size, d->head_size_v, d->dtype))
     return PKV_EUNSUPPORTED;
   const int esz = d->dtype == PKV_FP8_E4M3 ? 1 : 2;
@@ -455,7 +458,12 @@ int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void
                           partial_o, partial_lse, &p, &sms, &launch);
   if (rc != PKV_OK) return rc;
   if (num_tokens > 0 && out == nullptr) return PKV_EINVAL;
+  // the merge (in the kernel, or the second launch past 32 splits) reads the
+  // partials 16 bytes at a time and stores 4 bf16 outputs at a time, and
+  // counts rows in int
   if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return PKV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(partial_o) & 15u) != 0) return PKV_EINVAL;
+  if (static_cast<int64_t>(num_tokens) * num_q_heads > INT32_MAX) return PKV_EINVAL;
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, d->num_kv_heads,
                                                  max_query_len);
   if (num_tokens > 0 && (workspace == nullptr || workspace_bytes < need ||

@@ -8,6 +8,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_asymmetric_gb300 as pkv
 from paged_kv_asymmetric_gb300 import _build
@@ -108,6 +109,48 @@ def test_decode_rejects_bad_arguments(lib):
     assert _decode(lib, _desc(dtype=pkv.FP8_E4M3,
                               scale_mode=pkv.SCALE_TENSOR)) == pkv.EINVAL
     assert _decode(lib, d, T=0) == pkv.OK
+
+
+def _fused(lib, d, **kw):
+    a = dict(q=DUMMY, Hq=16, T=4, cache=DUMMY, bt=DUMMY, mb=4, sl=DUMMY,
+             qsl=DUMMY, B=2, mq=1, scale=0.1, ks=None, vs=None, S=4,
+             po=DUMMY, pl=DUMMY, ws=DUMMY, nws=1 << 20, out=DUMMY)
+    a.update(kw)
+    return lib.pkv_paged_attn_decode_fused(
+        a["q"], a["Hq"], a["T"], a["cache"], ctypes.byref(d), a["bt"], a["mb"], a["sl"],
+        a["qsl"], a["B"], a["mq"], ctypes.c_float(a["scale"]), a["ks"], a["vs"], a["S"],
+        a["po"], a["pl"], a["ws"], ctypes.c_size_t(a["nws"]), a["out"], None, None)
+
+
+def test_decode_rejects_misaligned_partials(lib):
+    d = _desc()
+    odd4 = ctypes.c_void_p(256 + 2)    # not even float-aligned
+    assert _decode(lib, d, po=odd4) == pkv.EINVAL
+    assert _decode(lib, d, pl=odd4) == pkv.EINVAL
+    # the fused merge reads the partials 16 bytes at a time and stores 4 bf16
+    # at a time; with no sequence the call stops after these checks
+    assert _fused(lib, d, B=0, po=ctypes.c_void_p(256 + 4)) == pkv.EINVAL
+    assert _fused(lib, d, B=0, out=ctypes.c_void_p(256 + 4)) == pkv.EINVAL
+    assert _fused(lib, d, B=0) == pkv.OK
+    assert _fused(lib, d, B=0, T=1 << 28, Hq=16) == pkv.EINVAL   # rows past int
+
+
+@pytest.mark.skipif(torch.cuda.is_available(),
+                    reason="a valid call would launch on the dummy pointers")
+def test_valid_shapes_pass_the_host_checks(lib):
+    """The shapes the GPU tests and the bench launch pass every host check:
+    without a GPU they end at the device query (PKV_ECUDA), not at a
+    rejection."""
+    bf = _desc(num_blocks=4096)
+    f8 = _desc(num_blocks=4096, block_size=64, dtype=pkv.FP8_E4M3,
+               scale_mode=pkv.SCALE_HEAD)
+    mla = _desc(num_blocks=4096, block_size=64, num_kv_heads=1, row_elems=576,
+                head_size=576, v_off=0, head_size_v=512)
+    assert _decode(lib, bf, T=32, B=32, mb=512, S=16) == pkv.ECUDA      # batched decode
+    assert _decode(lib, f8, T=96, B=24, mb=800, mq=4, S=16, ks=DUMMY,
+                   vs=DUMMY) == pkv.ECUDA                                # FP8 verify
+    assert _decode(lib, mla, Hq=16, T=1, B=1, mb=1600, S=304) == pkv.ECUDA   # MLA
+    assert _fused(lib, bf, T=32, B=32, mb=512, S=16) == pkv.ECUDA
 
 
 def test_prefill_rejects_bad_arguments(lib):
