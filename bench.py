@@ -8,16 +8,24 @@ algorithmic HBM bytes (every visible K|V row once per KV head, Q, O, block
 table, and the write's reads and writes) per second of device time.  The
 KV cache (419 MB) is larger than L2, so no flush is needed between steps.
 
-Also reported (``sub``): causal prefill TFLOP/s at 32,768 tokens (and
-131,072 with --long), the cache write of 32,768 tokens, speculative verify
-with an FP8 cache (16 x ~46K, q_len 4, 16 splits, 8 padded rows) and the
-MLA-shaped decode (100K context, 12 and 16 heads, batch 1 and 16).  Those are
-timed per launch with L2 flushed between launches.
+``roofline`` is the decode kernel alone: its launches back to back on the
+stream (no event between them), timed in a loop of their own after the
+headline loop, which runs with no event inside it.
+
+Also reported (``sub``): causal prefill TFLOP/s at 32,768 and 131,072 tokens
+and their cache writes, the 32,768-token prefill over an FP8 cache,
+speculative verify with an FP8 cache (16 x ~46K, q_len 4, 16 splits, 8
+padded rows) and the MLA-shaped decode (100K context, 12 and 16 heads, batch
+1 and 16).  Those are timed per launch with L2 flushed between launches.
+The prefill loads K/V tiles with TMA multicast between the two CTAs of a
+cluster, which is for single-GPU jobs only: a run with more than one rank
+takes no prefill measurement (and ``--only prefill`` refuses to run).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build:
 no third-party implementation of this path runs on GB300) on a bounded sample
-of the same workload.  With several GPUs (torchrun), every rank runs an
-independent replica (the path has no exchange step): ``scaling`` is weak.
+of the same workload.  With several GPUs (torchrun, ``--gpus N`` equal to
+its WORLD_SIZE), every rank runs an independent replica of the decode step
+(the path has no exchange step): ``scaling`` is weak.
 """
 from __future__ import annotations
 
@@ -78,6 +86,32 @@ def sum_over_ranks(x: float, ws: int, device=None) -> float:
     t = torch.tensor([float(x)], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
     return float(t.item())
+
+
+PREFILL_KINDS = ("prefill", "prefill_fp8")
+
+
+def require_single_gpu(ws: int, what: str) -> None:
+    """The prefill's K/V tiles are multicast by TMA between the two CTAs of a
+    cluster; that load is for jobs on one GPU only."""
+    if ws != 1:
+        raise RuntimeError(f"{what}: the cluster-multicast prefill runs in "
+                           f"single-GPU jobs only (world size {ws})")
+
+
+def sub_plan(args, ws: int):
+    """The sub-measurements of a run, in order, as (kind, name, size).
+    Prefill kinds appear only when the job has one rank."""
+    plan = []
+    if args.no_sub:
+        return plan
+    if ws == 1 and not args.skip_prefill:
+        plan += [("prefill", "prefill_32k", 32768),
+                 ("prefill_fp8", "prefill_fp8_32k", 32768),
+                 ("prefill", "prefill_128k", 131072)]
+    plan.append(("verify", "verify_fp8", 16))
+    plan += [("mla", f"mla_b{b}_h{h}", (b, h)) for b in (1, 16) for h in (12, 16)]
+    return plan
 
 
 def peaks():
@@ -301,6 +335,7 @@ def gpu_arm(args, ws, rank, local):
         torch.cuda.empty_cache()
 
     def prefill_sub(name, n_tokens):
+        require_single_gpu(ws, name)
         wk = wl.long_prefill(n_tokens, device=dev)
         dwk = wl.to_device(wk, device=dev)
         nw = wk.k_ctx.shape[0]
@@ -338,6 +373,7 @@ def gpu_arm(args, ws, rank, local):
     def prefill_fp8_sub(name, n_tokens):
         # the same causal prefill over an FP8 E4M3 cache (per-head scales):
         # the whole public call, the widening pass included
+        require_single_gpu(ws, name)
         wk = wl.make_workload(f"prefill-{n_tokens}-fp8", seq_lens=[n_tokens],
                               q_lens=[n_tokens], kv_dtype=wl.FP8,
                               scale_mode=wl.SCALE_HEAD, seed=0, device=dev)
@@ -365,6 +401,8 @@ def gpu_arm(args, ws, rank, local):
         torch.cuda.empty_cache()
 
     if args.only:
+        if args.only in PREFILL_KINDS:
+            require_single_gpu(ws, f"--only {args.only}")
         sampler = ClockSampler(local)
         sampler.start()
         if args.only == "prefill":
@@ -396,20 +434,15 @@ def gpu_arm(args, ws, rank, local):
     k_new = dw.k_ctx[new_idx].contiguous()
     v_new = dw.v_ctx[new_idx].contiguous()
     stream = torch.cuda.current_stream()
-    dec_ev = []
 
-    def step(record=False):
-        pkv.kv_cache_write(k_new, v_new, dw.slots_new, dw.cache)
-        if record:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+    def decode_only():
         pkv.paged_attn_decode(dw.q, dw.cache, dw.block_table, dw.seq_lens,
                               dw.query_start_loc, w.softmax_scale, 1, S,
                               partial_o=po, partial_lse=pl)
-        if record:
-            e1.record(stream)
-            dec_ev.append((e0, e1))
+
+    def step():
+        pkv.kv_cache_write(k_new, v_new, dw.slots_new, dw.cache)
+        decode_only()
         pkv.splitkv_reduce(po, pl, out=out)
 
     step_bytes = decode_bytes(w) + write_bytes(w, T)
@@ -422,14 +455,9 @@ def gpu_arm(args, ws, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    # The decode launches of every 4th step are timed with a pair of events
-    # (the roofline's average launch time).  An event record stands between
-    # two kernels in the stream, where it costs time and keeps the second
-    # from launching before the first ends; the other steps run as a user's
-    # would.
     t0.record(stream)
-    for i in range(args.steps):
-        step(record=(i % 4 == 0))
+    for _ in range(args.steps):
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -440,7 +468,20 @@ def gpu_arm(args, ws, rank, local):
     ms_step = ms_total_max / args.steps
     total_bytes = sum_over_ranks(step_bytes * args.steps, ws, dev)
     value = total_bytes / (ms_total_max * 1e-3) / 1e9
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+
+    # roofline: the decode kernel alone, its launches back to back with no
+    # event between them (the 419 MB cache is larger than L2, so every
+    # launch reads from HBM); average duration = loop time / launches
+    n_roof = max(50, args.steps)
+    for _ in range(3):
+        decode_only()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n_roof):
+        decode_only()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = t0.elapsed_time(t1) / n_roof
     dec_alg = decode_bytes(w)
     dec_gbs = dec_alg / (dec_ms * 1e-3) / 1e9
 
@@ -521,21 +562,24 @@ def gpu_arm(args, ws, rank, local):
     if not torch.equal(h_outs[(args.steps - 1) & 1], outs[(args.steps - 1) & 1].cpu()):
         raise RuntimeError("e2e output mismatch")
 
-    if not args.no_sub:
-        if not args.skip_prefill:
-            prefill_sub("prefill_32k", 32768)
-            prefill_fp8_sub("prefill_fp8_32k", 32768)
-            if args.long:
-                prefill_sub("prefill_128k", 131072)
-        wv = wl.verify_fp8(device=dev)
-        attn_decode_sub("verify_fp8", wv, 16, time_write=True)
-        del wv
-        for b in (1, 16):
-            for h in (12, 16):
-                wm = wl.mla_decode(batch=b, heads=h, device=dev)
-                s = pkv.decode_suggest_splits(b, h, 1, 1, 100000, 64)
-                attn_decode_sub(f"mla_b{b}_h{h}", wm, s)
-                del wm
+    for kind, name, size in sub_plan(args, ws):
+        if kind == "prefill":
+            prefill_sub(name, size)
+        elif kind == "prefill_fp8":
+            prefill_fp8_sub(name, size)
+        elif kind == "verify":
+            wv = wl.verify_fp8(device=dev)
+            attn_decode_sub(name, wv, size, time_write=True)
+            del wv
+        elif kind == "mla":
+            b, h = size
+            wm = wl.mla_decode(batch=b, heads=h, device=dev)
+            s = pkv.decode_suggest_splits(b, h, 1, 1, 100000, 64)
+            attn_decode_sub(name, wm, s)
+            del wm
+    if ws > 1 and not args.no_sub:
+        sub["prefill"] = ("not measured: the cluster-multicast prefill runs in "
+                          "single-GPU jobs only")
     clocks = sampler.stop()
 
     traffic = traffic_record("decode_bf16_192")
@@ -544,7 +588,9 @@ def gpu_arm(args, ws, rank, local):
             "frac": dec_gbs / hbm, "peak_kind": pk_kind,
             "traffic": traffic,
             "algorithmic_bytes_per_launch": dec_alg,
-            "avg_launch_ms": dec_ms}
+            "avg_launch_ms": dec_ms, "launches_timed": n_roof,
+            "timing": "back-to-back launches of the decode kernel alone, "
+                      "CUDA events around the loop"}
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -651,7 +697,6 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--long", action="store_true", help="add the 131,072-token prefill")
     ap.add_argument("--no-sub", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--only", choices=["prefill", "prefill_fp8", "verify", "mla", "decode"],
@@ -665,6 +710,9 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=30.0)
     args = ap.parse_args(argv)
     ws, rank, local = dist_info()
+    if args.gpus < 1 or args.gpus != ws:
+        ap.error(f"--gpus {args.gpus} does not match the job's world size {ws}: "
+                 "run N ranks with torch.distributed.run --nproc-per-node N")
     if args.impl == "reference":
         init_dist(ws, "gloo")
         res = reference_arm(args, ws, rank)

@@ -160,7 +160,11 @@ int pkv_kv_cache_write(const void *key, int64_t key_tok_stride,
  * This build: bf16 cache, head_size 192 and head_size_v 128, num_q_heads /
  * num_kv_heads dividing 128, block_size a power of two >= 8, K at a
  * 64-element column offset; otherwise PKV_EUNSUPPORTED.  PKV_EINVAL for null
- * pointers, softmax_scale <= 0 or inconsistent sizes.
+ * pointers, softmax_scale <= 0 or inconsistent sizes, and when q, cache or
+ * out is not device memory of the current device (pinned or mapped host
+ * memory, managed memory, another GPU's memory): the kernel's tensor maps
+ * and its K/V loads, multicast to the two CTAs of a cluster, cover this
+ * GPU's own memory only.
  */
 int pkv_paged_attn_prefill(const void *q, int num_q_heads, int num_tokens,
                            const void *cache, const pkv_cache_desc *d,
@@ -202,8 +206,9 @@ size_t pkv_prefill_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
  * 256-byte aligned, overwritten by the call; overlapping calls must not
  * share it.  An out-of-range page id is skipped (read as zeros) and
  * recorded as PKV_EDEV_RANGE.  Status codes as in pkv_paged_attn_prefill;
- * PKV_EINVAL also for a non-FP8 cache or a missing, misaligned or too small
- * workspace.
+ * PKV_EINVAL also for a non-FP8 cache, a missing, misaligned or too small
+ * workspace, or a q, cache, workspace or out that is not device memory of
+ * the current device (checked before the first pass is launched).
  */
 int pkv_paged_attn_prefill_fp8(const void *q, int num_q_heads, int num_tokens,
                                const void *cache, const pkv_cache_desc *d,
@@ -319,20 +324,29 @@ int pkv_paged_attn_decode_fused(const void *q, int num_q_heads, int num_tokens,
 
 /*
  * pkv_paged_attn_decode_fused_noalloc -- pkv_paged_attn_decode_fused
- * without a caller workspace.  The pages have no counterpart: this entry
- * exists for callers that have no device allocator at hand.  Its counters
- * live in a fixed array of 65536 32-bit counters (256 KB) in this library's
- * own device memory, one array per device, whose address is looked up once
- * per device; nothing is allocated.  After every argument has been checked,
- * each call zero-fills, on `stream`, the counters it is about to use (so a
- * call after a device error needs no clearing), then launches as
- * pkv_paged_attn_decode_fused does.  All calls on a device share that one
- * array: calls that overlap in time (on different streams or host threads)
- * race on it and give wrong results, so serialise them.
- * PKV_EINVAL also when pkv_decode_workspace_bytes(num_seqs, num_q_heads,
- * d->num_kv_heads, max_query_len) exceeds 256 KB (more than 65536 counters);
- * other arguments, results and status codes as in
- * pkv_paged_attn_decode_fused.
+ * without a caller workspace.  The pages have no counterpart.  It serves
+ * callers that cannot allocate device memory for the counters: a serving
+ * engine that hands all free GPU memory to its KV-cache pool at start-up
+ * and takes no further allocation during a step, or a plain C host program
+ * that links only this library and has no allocator of its own.  Its
+ * counters live in a fixed array of 65536 32-bit counters (256 KB) in this
+ * library's own device memory, one array per device, held by every device
+ * that loads the library until the process exits; nothing is allocated.
+ * Set-up: the first call on a device looks up that device's array address
+ * (cudaGetSymbolAddress, with the device current; a failure returns
+ * PKV_ECUDA), so make that first call before any stream capture.  After
+ * every argument has been checked, each call zero-fills, on `stream`, the
+ * counters it is about to use (so a call after a device error needs no
+ * clearing), then launches as pkv_paged_attn_decode_fused does.  All calls
+ * on a device share that one array, which keeps the last call's contents:
+ * calls that overlap in time (on different streams or host threads) race
+ * on it and give wrong results, so serialise them.
+ * PKV_EINVAL also when num_splits <= 32 (the merge runs inside the decode
+ * kernel and uses the counters) and pkv_decode_workspace_bytes(num_seqs,
+ * num_q_heads, d->num_kv_heads, max_query_len) exceeds 256 KB (more than
+ * 65536 counters).  Past 32 splits the merge is a second launch that uses
+ * no counter, so no size limit applies.  Other arguments, results and
+ * status codes as in pkv_paged_attn_decode_fused.
  */
 int pkv_paged_attn_decode_fused_noalloc(const void *q, int num_q_heads,
                                         int num_tokens, const void *cache,

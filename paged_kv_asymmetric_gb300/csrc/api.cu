@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "common.cuh"
@@ -139,6 +140,26 @@ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// Whether every pointer is plain device memory of the current device.  The
+// prefill's tensor maps and its cluster-multicast TMA loads must cover this
+// GPU's own memory only: pinned or mapped host memory, managed memory and a
+// peer GPU's memory are refused before any tensor map is encoded.
+int check_local_device(std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  for (const void* ptr : ptrs) {
+    cudaPointerAttributes a{};
+    e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();  // not a pointer CUDA knows: clear the error
+      return PKV_EINVAL;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return PKV_EINVAL;
+  }
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -219,6 +240,10 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
       d->k_off % 64 != 0 || d->v_off % 8 != 0)
     return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
+  // q and the cache are read through tensor maps (K/V boxes multicast to
+  // both CTAs of a cluster), out is written: all must be this GPU's memory
+  rc = check_local_device({q, cache, out});
+  if (rc != PKV_OK) return rc;
   int* err = nullptr;
   int sms = 0;
   rc = device_info(&err, &sms);
@@ -311,6 +336,11 @@ int pkv_paged_attn_prefill_fp8(const void* q, int num_q_heads, int num_tokens,
   if (!aligned16(cache) || !aligned16(q) || (d->row_elems * 2) % 16 != 0 ||
       d->k_off % 64 != 0 || d->v_off % 8 != 0)
     return PKV_EUNSUPPORTED;
+  // the widened pages (workspace) and q are read through tensor maps by the
+  // prefill: every buffer must be this GPU's memory, checked before the
+  // first launch
+  rc = check_local_device({q, cache, workspace, out});
+  if (rc != PKV_OK) return rc;
   int* err = nullptr;
   int sms = 0;
   rc = device_info(&err, &sms);
@@ -523,10 +553,14 @@ int pkv_paged_attn_decode_fused_noalloc(const void* q, int num_q_heads, int num_
                                         float* partial_lse, void* out, float* lse_out,
                                         pkv_stream_t stream) {
   if (d == nullptr) return PKV_EINVAL;
-  // the sizes must fit the fixed counter array
+  // The counters serve the in-kernel merge only (up to kFusedMaxSplits
+  // splits); there the sizes must fit the fixed counter array.  Past it the
+  // merge is a second launch that uses no counter, and any size is taken.
+  const size_t array_bytes = sizeof(int) * static_cast<size_t>(kNoAllocCounters);
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, d->num_kv_heads,
                                                  max_query_len);
-  if (need > sizeof(int) * static_cast<size_t>(kNoAllocCounters)) return PKV_EINVAL;
+  const bool in_kernel_merge = num_splits <= pkv::kFusedMaxSplits;
+  if (in_kernel_merge && need > array_bytes) return PKV_EINVAL;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -546,7 +580,7 @@ int pkv_paged_attn_decode_fused_noalloc(const void* q, int num_q_heads, int num_
                            max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                            max_query_len, softmax_scale, k_scale, v_scale, num_splits,
                            partial_o, partial_lse, counters,
-                           sizeof(int) * static_cast<size_t>(kNoAllocCounters), out,
+                           in_kernel_merge || need <= array_bytes ? array_bytes : need, out,
                            lse_out, stream, /*clear=*/true);
 }
 

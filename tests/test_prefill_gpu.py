@@ -92,3 +92,47 @@ def test_prefill_32k_sampled():
     toks = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 32767],
                                      rng.integers(0, 32768, 10)])).astype(np.int32)
     _run_and_check(w, tokens=toks, seqs=[0])
+
+
+def _raw_prefill(q_ptr, cache_ptr, out_ptr, dw):
+    """pkv_paged_attn_prefill through the C ABI with the given raw pointers
+    (the binding itself takes CUDA tensors only)."""
+    import ctypes
+    w = dw.w
+    return pkv.load().pkv_paged_attn_prefill(
+        ctypes.c_void_p(q_ptr), w.num_q_heads, w.num_tokens, ctypes.c_void_p(cache_ptr),
+        ctypes.byref(dw.cache.desc), ctypes.c_void_p(dw.block_table.data_ptr()),
+        int(dw.block_table.shape[1]), ctypes.c_void_p(dw.seq_lens.data_ptr()),
+        ctypes.c_void_p(dw.query_start_loc.data_ptr()), w.num_seqs,
+        float(w.softmax_scale), None, None, ctypes.c_void_p(out_ptr),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_prefill_rejects_memory_of_other_kinds():
+    """The prefill's tensor maps (K/V tiles multicast to the two CTAs of a
+    cluster) must cover this GPU's own memory: a pinned host buffer passed
+    as the cache, q or out is refused with PKV_EINVAL and nothing runs."""
+    w = wl.tiny("prefill")
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    T, Hq = w.num_tokens, w.num_q_heads
+    out = torch.full((T, Hq, w.head_size_v), 7.0, dtype=torch.bfloat16, device="cuda")
+    nbytes = dw.cache.data.numel() * dw.cache.data.element_size()
+    host_cache = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host_cache.copy_(dw.cache.data.cpu())
+    host_q = dw.q.cpu().pin_memory()
+    host_out = torch.zeros(T, Hq, w.head_size_v, dtype=torch.bfloat16, pin_memory=True)
+    torch.cuda.synchronize()
+    q, c, o = dw.q.data_ptr(), dw.cache.data.data_ptr(), out.data_ptr()
+    for args in ((q, host_cache.data_ptr(), o), (host_q.data_ptr(), c, o),
+                 (q, c, host_out.data_ptr())):
+        assert _raw_prefill(*args, dw) == pkv.EINVAL
+    torch.cuda.synchronize()
+    assert (out.float() == 7.0).all()           # nothing was launched
+    assert (host_out.float() == 0.0).all()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+    # the same call on device memory runs
+    assert _raw_prefill(q, c, o, dw) == pkv.OK
+    torch.cuda.synchronize()
+    ref, _ = gpu_path.oracle_rows(w)
+    refs.assert_close(gpu_path.host(out), ref, **gpu_path.BF16_TOL)

@@ -1,8 +1,9 @@
 """The no-allocation fused decode (pkv_paged_attn_decode_fused_noalloc): its
 counters live in the library's own fixed device array, so it takes no
 workspace.  Two calls in a row give, bit for bit, what the workspace entry
-pkv_paged_attn_decode_fused gives on the same inputs, and sizes needing more
-than 65536 counters are rejected before anything is launched.  The file is
+pkv_paged_attn_decode_fused gives on the same inputs, and, when the merge
+runs inside the decode kernel (up to 32 splits), sizes needing more than
+65536 counters are rejected before anything is launched.  The file is
 named to be collected last, so it also runs after every other GPU test has
 used the library in the same process."""
 from __future__ import annotations
@@ -106,5 +107,10 @@ def test_noalloc_rejects_more_than_65536_counters():
             pkv.paged_attn_decode_fused(
                 q, dw.cache, bt, sl, qsl, w.softmax_scale, 1, 4, ws,
                 k_scale=dw.k_scale, v_scale=dw.v_scale)
+    # past 32 splits the merge is a second launch that uses no counter: the
+    # same oversized batch is taken
+    q, bt, sl, qsl = _empty_batch(dw, fit + 1)
+    pkv.paged_attn_decode_fused_noalloc(q, dw.cache, bt, sl, qsl, w.softmax_scale,
+                                        1, 40, k_scale=dw.k_scale, v_scale=dw.v_scale)
     torch.cuda.synchronize()
     assert gpu_path.device_error() == pkv.EDEV_NONE
