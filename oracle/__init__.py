@@ -74,7 +74,7 @@ def _load():
         lib.oracle_kv_cache_write.restype = i32
         lib.oracle_paged_attn.argtypes = [
             P, i32, i32, P, ctypes.POINTER(CacheDesc), P, i32, P, P, i32,
-            ctypes.c_float, P, P, P, i32, i32, i32, P, P, P]
+            ctypes.c_float, P, P, P, i32, i32, i32, i32, P, P, P]
         lib.oracle_paged_attn.restype = i32
         lib.oracle_splitkv_reduce.argtypes = [P, P, i32, i64, i32, P, P, P, i32]
         lib.oracle_splitkv_reduce.restype = None
@@ -146,9 +146,12 @@ def kv_cache_write(key_bits, value_bits, slot_mapping, cache, d: CacheDesc,
 def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
                seq_lens, query_start_loc, softmax_scale, k_scale=None,
                v_scale=None, tokens=None, num_splits=0, split=-1,
-               threads=1, sinks=None):
+               threads=1, sinks=None, split_ranges=0):
     """Returns (out [n, Hq, dv] float64, lse [n, Hq] float64) for the query
-    tokens listed in ``tokens`` (all tokens when None).  ``threads`` > 1
+    tokens listed in ``tokens`` (all tokens when None).  ``split`` >= 0 gives
+    the partial of that segment: equal segments of ``num_splits``, or, with
+    ``split_ranges`` = W > 0, the balanced ranges of W (see segment_pages in
+    pkv_oracle.c).  ``threads`` > 1
     splits the token list over Python threads (the C call releases the
     GIL); the arithmetic of each row is unchanged.  ``sinks`` (float32 [Hq],
     or None): one attention-sink logit per query head, for whole rows
@@ -180,7 +183,8 @@ def paged_attn(q_bits, num_q_heads, cache, d: CacheDesc, block_table,
             _ptr(q_bits), num_q_heads, T, _ptr(cache), ctypes.byref(d),
             _ptr(bt), max_blocks, _ptr(sl), _ptr(qsl), int(sl.shape[0]),
             float(softmax_scale), _ptr(kscale), _ptr(vscale), _ptr(sub),
-            hi - lo, int(num_splits), int(split), _ptr(o), _ptr(ls), _ptr(snk))
+            hi - lo, int(num_splits), int(split), int(split_ranges), _ptr(o),
+            _ptr(ls), _ptr(snk))
 
     if threads <= 1 or n < 2:
         rcs = [run(0, n)]

@@ -288,24 +288,83 @@ static void attend_row(const uint16_t *q_row, const void *cache,
     *lse = m + log(l);
 }
 
+/* Page range [*plo, *phi) of segment `split` of sequence b, the pages of
+ * the sequence being P = ceil(L / block_size).
+ *
+ * Equal segments (split_ranges == 0; the split-KV of [MiMo-2xRTX] "What the
+ * kernels do" with page-aligned segments): pps = ceil(P / num_splits) pages
+ * per segment, segment s = [s * pps, min((s + 1) * pps, P)).
+ *
+ * Balanced ranges (split_ranges = W > 0; split selection from the sequence
+ * lengths on the device, [PR50371] discussion): the pages of all sequences
+ * are laid end to end in sequence order, sequence b starting at global page
+ * G_b = sum of P over the sequences before it, Ptot pages in all.  That line
+ * is cut into ranges of R pages, R = max(ceil(Ptot / W), Rmin, 1), where
+ * Rmin keeps every sequence within num_splits segments: Rmin = Ptot when
+ * num_splits is 1, else floor(max(Pmax - 2, 0) / (num_splits - 1)) + 1
+ * (Pmax the largest P; a sequence of P >= 2 pages meets at most
+ * floor((P - 2) / R) + 2 ranges).  Segment s of sequence b is the part of
+ * the sequence inside range floor(G_b / R) + s, in the sequence's own page
+ * numbers; it is empty when that range holds none of its pages. */
+static void segment_pages(const int32_t *seq_lens, int num_seqs, int b,
+                          int block_size, int num_splits, int split_ranges,
+                          int split, int64_t *plo, int64_t *phi)
+{
+    int64_t P = ((int64_t)seq_lens[b] + block_size - 1) / block_size;
+    if (split_ranges <= 0) {
+        int64_t pps = (P + num_splits - 1) / num_splits;
+        int64_t lo = (int64_t)split * pps, hi = lo + pps;
+        *plo = lo < P ? lo : P;
+        *phi = hi < P ? hi : P;
+    } else {
+        int64_t Ptot = 0, Pmax = 0, G = 0, R, Rmin, r, lo, hi;
+        int i;
+        for (i = 0; i < num_seqs; ++i) {
+            int64_t Pi = ((int64_t)seq_lens[i] + block_size - 1) / block_size;
+            if (i < b)
+                G += Pi;
+            Ptot += Pi;
+            if (Pi > Pmax)
+                Pmax = Pi;
+        }
+        R = (Ptot + split_ranges - 1) / split_ranges;
+        if (num_splits == 1)
+            Rmin = Ptot;
+        else
+            Rmin = (Pmax > 2 ? Pmax - 2 : 0) / (num_splits - 1) + 1;
+        if (R < Rmin)
+            R = Rmin;
+        if (R < 1)
+            R = 1;
+        r = G / R + split;            /* the range of segment `split` */
+        lo = r * R > G ? r * R : G;   /* its global pages, clipped to b */
+        hi = (r + 1) * R < G + P ? (r + 1) * R : G + P;
+        if (hi < lo)
+            hi = lo;
+        *plo = lo - G;
+        *phi = hi - G;
+    }
+}
+
 /* Attention over the paged cache for a list of query tokens.
  *
  * tokens[0 .. n_tokens) selects the query tokens (global token indices);
  * tokens == NULL means all num_tokens of them.  q is [num_tokens][Hq][dk]
  * bf16 (raw bits), out_o is [n][Hq][dv] and out_lse is [n][Hq], binary64.
  * split < 0 computes the whole row; otherwise the partial of segment
- * `split` of `num_splits` (see attend_row).  Returns 0, or -1 when a token
- * index is outside every sequence.  sinks (NULL: none) holds one sink logit
- * per query head; it enters whole rows only (split < 0): a segment's partial
- * is sink-free and the merge adds the sink once. */
+ * `split` of `num_splits`, cut as segment_pages describes (equal segments
+ * when split_ranges is 0, balanced ranges otherwise).  Returns 0, or -1
+ * when a token index is outside every sequence.  sinks (NULL: none) holds
+ * one sink logit per query head; it enters whole rows only (split < 0): a
+ * segment's partial is sink-free and the merge adds the sink once. */
 int oracle_paged_attn(const uint16_t *q, int num_q_heads, int num_tokens,
                       const void *cache, const oracle_cache_desc *d,
                       const int32_t *block_table, int max_blocks_per_seq,
                       const int32_t *seq_lens, const int32_t *query_start_loc,
                       int num_seqs, float softmax_scale, const float *k_scale,
                       const float *v_scale, const int32_t *tokens, int n_tokens,
-                      int num_splits, int split, double *out_o, double *out_lse,
-                      const float *sinks)
+                      int num_splits, int split, int split_ranges, double *out_o,
+                      double *out_lse, const float *sinks)
 {
     int n = tokens ? n_tokens : num_tokens;
     int G = num_q_heads / d->num_kv_heads;
@@ -330,13 +389,9 @@ int oracle_paged_attn(const uint16_t *q, int num_q_heads, int num_tokens,
         lo = 0;
         hi = n_vis;
         if (split >= 0) {
-            int64_t P = (L + d->block_size - 1) / d->block_size;
-            int64_t pps = (P + num_splits - 1) / num_splits;
-            int64_t plo = (int64_t)split * pps, phi = plo + pps;
-            if (phi > P)
-                phi = P;
-            if (plo > P)
-                plo = P;
+            int64_t plo, phi;
+            segment_pages(seq_lens, num_seqs, b, d->block_size, num_splits,
+                          split_ranges, split, &plo, &phi);
             lo = plo * d->block_size;
             if (phi * d->block_size < hi)
                 hi = phi * d->block_size;

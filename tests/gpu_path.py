@@ -49,10 +49,12 @@ def host(t):
     return t.detach().float().cpu().numpy()
 
 
-def oracle_rows(w, tokens=None, seqs=None, num_splits=0, split=-1, sinks=None):
+def oracle_rows(w, tokens=None, seqs=None, num_splits=0, split=-1, sinks=None,
+                split_ranges=0):
     cache = refs.oracle_cache(w, seqs=seqs)
     return refs.oracle_attn(w, cache, tokens=tokens, num_splits=num_splits,
-                            split=split, threads=THREADS, sinks=sinks)
+                            split=split, threads=THREADS, sinks=sinks,
+                            split_ranges=split_ranges)
 
 
 def tokens_of(w, seqs):

@@ -52,12 +52,12 @@ def oracle_cache(w: wl.Workload, seqs=None) -> np.ndarray:
 
 
 def oracle_attn(w: wl.Workload, cache: np.ndarray, tokens=None,
-                num_splits=0, split=-1, threads=1, sinks=None):
+                num_splits=0, split=-1, threads=1, sinks=None, split_ranges=0):
     return oracle.paged_attn(
         bf16_bits(w.q), w.num_q_heads, cache, oracle_desc(w), w.block_table,
         w.seq_lens, w.query_start_loc, w.softmax_scale, w.k_scale, w.v_scale,
         tokens=tokens, num_splits=num_splits, split=split, threads=threads,
-        sinks=sinks)
+        sinks=sinks, split_ranges=split_ranges)
 
 
 # ------------------------------------------------------------ references --

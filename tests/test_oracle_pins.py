@@ -398,3 +398,104 @@ def test_reduce_closed_forms():
     # every segment empty: 0, lse -inf, no NaN
     out, lse = oracle.splitkv_reduce(o2, np.full((3, 5), -np.inf, np.float32))
     assert (out == 0).all() and np.isneginf(lse).all()
+
+
+# ------------------------------------------ segment boundaries, by example --
+
+def _segment_key_counts(w, S, W=0):
+    """Visible keys of each segment for each query row: with a zero query
+    every score is 0 and a segment's lse is log(its key count) exactly."""
+    w.q.zero_()
+    cache = refs.oracle_cache(w)
+    rows = []
+    for s in range(S):
+        _, l = refs.oracle_attn(w, cache, num_splits=S, split=s, split_ranges=W)
+        c = np.where(np.isfinite(l[:, 0]), np.exp(l[:, 0]), 0.0)
+        rows.append(np.rint(c).astype(int))
+        assert np.allclose(c, rows[-1], atol=1e-9)
+    return np.stack(rows, 1)   # [token, segment]
+
+
+def test_equal_segments_closed_form():
+    """211 keys in pages of 16 are 14 pages; 5 segments of ceil(14 / 5) = 3
+    pages hold 3, 3, 3, 3 and 2 pages, i.e. 48, 48, 48, 48 and the last 19
+    keys.  50 keys (4 pages) over 8 segments: one page each, then 4 empty
+    ones."""
+    w = wl.make_workload("seg", seq_lens=[211], q_lens=[1], seed=30)
+    assert _segment_key_counts(w, 5).tolist() == [[48, 48, 48, 48, 19]]
+    w = wl.make_workload("seg", seq_lens=[50], q_lens=[1], seed=30)
+    assert _segment_key_counts(w, 8).tolist() == [[16, 16, 16, 2, 0, 0, 0, 0]]
+
+
+def test_balanced_ranges_closed_forms():
+    """Balanced ranges, worked by hand.  Keys 100, 50, 30 in pages of 10 are
+    10, 5 and 3 pages, laid end to end at global pages 0, 10 and 15 (18 in
+    all)."""
+    kw = dict(seq_lens=[100, 50, 30], q_lens=[1, 1, 1], block_size=10, seed=31)
+    # W = 4: R = ceil(18 / 4) = 5 (Rmin = floor(8 / 3) + 1 = 3); ranges
+    # [0,5) [5,10) [10,15) [15,18): sequence 0 is two ranges of 50 keys,
+    # sequences 1 and 2 one range each
+    w = wl.make_workload("bal", **kw)
+    assert _segment_key_counts(w, 4, W=4).tolist() == [
+        [50, 50, 0, 0], [50, 0, 0, 0], [30, 0, 0, 0]]
+    # W = 3: R = 6; ranges [0,6) [6,12) [12,18): sequence 0 takes 6 + 4
+    # pages, sequence 1 (pages 10..14) 2 pages of range 1 and 3 of range 2,
+    # sequence 2 the last 3 pages of range 2
+    w = wl.make_workload("bal", **kw)
+    assert _segment_key_counts(w, 4, W=3).tolist() == [
+        [60, 40, 0, 0], [20, 30, 0, 0], [30, 0, 0, 0]]
+    # W = 1: one range, one segment per sequence
+    w = wl.make_workload("bal", **kw)
+    assert _segment_key_counts(w, 4, W=1).tolist() == [
+        [100, 0, 0, 0], [50, 0, 0, 0], [30, 0, 0, 0]]
+
+
+def test_balanced_ranges_keep_within_max_splits():
+    """One long and one short sequence with many ranges asked for: keys 1000
+    and 10 in pages of 10 are 100 + 1 pages.  W = 101 would give R = 1, but
+    with at most 4 segments per sequence R grows to Rmin = floor(98 / 3) + 1
+    = 33: ranges [0,33) [33,66) [66,99) [99,132).  The short sequence (global
+    page 100) lies in range 3, its segment 0.  With 1 segment allowed, R is
+    the whole line."""
+    kw = dict(seq_lens=[1000, 10], q_lens=[1, 1], block_size=10, seed=32)
+    w = wl.make_workload("cap", **kw)
+    assert _segment_key_counts(w, 4, W=101).tolist() == [
+        [330, 330, 330, 10], [10, 0, 0, 0]]
+    w = wl.make_workload("cap", **kw)
+    assert _segment_key_counts(w, 1, W=101).tolist() == [[1000], [10]]
+
+
+def test_balanced_ranges_causal_rows_and_empty_sequences():
+    """Rows of a 3-token query see 209, 210 and 211 keys; empty sequences
+    (seq_len 0) hold no page and have no segment.  Keys 211 (14 pages of 16),
+    0, 40 (3 pages), 0: 17 pages; W = 4 gives R = 5 (Rmin = floor(12 / 4) + 1
+    = 4).  Sequence 0: ranges [0,5) [5,10) [10,15) -> 80, 80 and the rest
+    (4 pages: 51, 50, 49 keys for its three rows); sequence 2 (global pages
+    14..16): 1 page in range 2, 2 pages in range 3 -> 16 and 24 keys."""
+    w = wl.make_workload("cz", seq_lens=[211, 0, 40, 0], q_lens=[3, 2, 1, 1],
+                         block_size=16, seed=33)
+    got = _segment_key_counts(w, 5, W=4)
+    assert got.tolist() == [[80, 80, 49, 0, 0], [80, 80, 50, 0, 0],
+                            [80, 80, 51, 0, 0], [0] * 5, [0] * 5,
+                            [16, 24, 0, 0, 0], [0] * 5]
+
+
+@pytest.mark.parametrize("W", [1, 3, 7, 152, 1000])
+def test_balanced_partials_merge_to_whole(W):
+    """Whatever the cut, the merged segments are the whole row."""
+    w = wl.make_workload("bm", seq_lens=[300, 17, 0, 129, 64], q_lens=[4, 4, 4, 1, 2],
+                         block_size=16, seed=34)
+    cache = refs.oracle_cache(w)
+    whole, wl_lse = refs.oracle_attn(w, cache)
+    S = 8
+    po = np.zeros((S,) + whole.shape, np.float32)
+    pl = np.zeros((S,) + wl_lse.shape, np.float32)
+    for s in range(S):
+        po[s], pl[s] = refs.oracle_attn(w, cache, num_splits=S, split=s,
+                                        split_ranges=W)
+    T, H, dv = whole.shape
+    out, lse = oracle.splitkv_reduce(po.reshape(S, T * H, dv), pl.reshape(S, T * H))
+    assert np.allclose(out.reshape(whole.shape), whole, atol=1e-6, rtol=1e-6)
+    fin = np.isfinite(wl_lse.reshape(-1))
+    assert (np.isfinite(lse) == fin).all()
+    assert np.allclose(lse[fin], wl_lse.reshape(-1)[fin], atol=1e-5)
