@@ -3,7 +3,8 @@
 Headline step (``value``): one batched decode step of the library's hot path
 on the batched-decode workload (32 sequences, context U[2048, 8192], q_len 1,
 16 query / 4 KV heads, K 192 / V 128, block 16, bf16): write the step's new
-K/V into the paged cache, split-KV decode, merge.  ``value`` is the step's
+K/V into the paged cache, split-KV decode with balanced ranges (at most 16
+segments per sequence, cut on the device from seq_lens), merge.  ``value`` is the step's
 algorithmic HBM bytes (every visible K|V row once per KV head, Q, O, block
 table, and the write's reads and writes) per second of device time.  The
 KV cache (419 MB) is larger than L2, so no flush is needed between steps.
@@ -290,7 +291,7 @@ def gpu_arm(args, ws, rank, local):
     sub = {}
     reps = max(3, args.sub_reps)
 
-    def attn_decode_sub(name, wk, splits, time_write=False):
+    def attn_decode_sub(name, wk, splits, time_write=False, balanced=False):
         dwk = wl.to_device(wk, device=dev)
 
         def wr():
@@ -310,11 +311,17 @@ def gpu_arm(args, ws, rank, local):
         outk = torch.empty(Tk, Hk, dvk, dtype=torch.bfloat16, device=dev)
 
         def dec():
-            pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
-                                  dwk.seq_lens, dwk.query_start_loc,
-                                  wk.softmax_scale, wk.max_query_len, splits,
-                                  partial_o=pok, partial_lse=plk,
-                                  k_scale=dwk.k_scale, v_scale=dwk.v_scale)
+            if balanced:
+                pkv.paged_attn_decode_balanced(
+                    dwk.q, dwk.cache, dwk.block_table, dwk.seq_lens, dwk.query_start_loc,
+                    wk.softmax_scale, wk.max_query_len, splits, 0, partial_o=pok,
+                    partial_lse=plk, k_scale=dwk.k_scale, v_scale=dwk.v_scale)
+            else:
+                pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
+                                      dwk.seq_lens, dwk.query_start_loc,
+                                      wk.softmax_scale, wk.max_query_len, splits,
+                                      partial_o=pok, partial_lse=plk,
+                                      k_scale=dwk.k_scale, v_scale=dwk.v_scale)
 
         def red():
             pkv.splitkv_reduce(pok, plk, out=outk)
@@ -327,6 +334,8 @@ def gpu_arm(args, ws, rank, local):
         mrs, _ = time_launches(red_sink, reps, 2, flush)
         b = decode_bytes(wk)
         sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
+                     "segments": "balanced ranges (at most splits)" if balanced
+                     else "equal segments",
                      "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
                      "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
                      "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm,
@@ -411,14 +420,15 @@ def gpu_arm(args, ws, rank, local):
             prefill_fp8_sub(f"prefill_fp8_{args.prefill_tokens}", args.prefill_tokens)
         elif args.only == "verify":
             attn_decode_sub("verify_fp8", wl.verify_fp8(device=dev), args.splits or 16,
-                            time_write=True)
+                            time_write=True, balanced=True)
         elif args.only == "mla":
             s = pkv.decode_suggest_splits(1, 16, 1, 1, 100000, 64)
             attn_decode_sub("mla_b1_h16", wl.mla_decode(batch=1, heads=16,
                                                         device=dev), args.splits or s)
         elif args.only == "decode":
             wd = wl.batched_decode(device=dev)
-            attn_decode_sub("batched_decode", wd, args.splits or wd.max_splits)
+            attn_decode_sub("batched_decode", wd, args.splits or wd.max_splits,
+                            balanced=True)
         return {"only": args.only, "sub": sub, "clocks": sampler.stop()}
 
     # ---------------- headline: batched decode step -------------------
@@ -436,9 +446,9 @@ def gpu_arm(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def decode_only():
-        pkv.paged_attn_decode(dw.q, dw.cache, dw.block_table, dw.seq_lens,
-                              dw.query_start_loc, w.softmax_scale, 1, S,
-                              partial_o=po, partial_lse=pl)
+        pkv.paged_attn_decode_balanced(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                                       dw.query_start_loc, w.softmax_scale, 1, S, 0,
+                                       partial_o=po, partial_lse=pl)
 
     def step():
         pkv.kv_cache_write(k_new, v_new, dw.slots_new, dw.cache)
@@ -532,9 +542,9 @@ def gpu_arm(args, ws, rank, local):
         stream.wait_event(in_ready[b])
         stream.wait_event(out_read[b])
         pkv.kv_cache_write(d_k, d_v, d_slots, dw.cache)
-        pkv.paged_attn_decode(d_q, dw.cache, d_bt, d_sl, d_qsl,
-                              w.softmax_scale, 1, S, partial_o=po,
-                              partial_lse=pl)
+        pkv.paged_attn_decode_balanced(d_q, dw.cache, d_bt, d_sl, d_qsl,
+                                       w.softmax_scale, 1, S, 0, partial_o=po,
+                                       partial_lse=pl)
         in_free[b].record(stream)
         pkv.splitkv_reduce(po, pl, out=outs[b])
         out_ready[b].record(stream)
@@ -569,7 +579,7 @@ def gpu_arm(args, ws, rank, local):
             prefill_fp8_sub(name, size)
         elif kind == "verify":
             wv = wl.verify_fp8(device=dev)
-            attn_decode_sub(name, wv, size, time_write=True)
+            attn_decode_sub(name, wv, size, time_write=True, balanced=True)
             del wv
         elif kind == "mla":
             b, h = size
@@ -583,7 +593,7 @@ def gpu_arm(args, ws, rank, local):
     clocks = sampler.stop()
 
     traffic = traffic_record("decode_bf16_192")
-    roof = {"kernel": "decode_kernel<192,128,bf16>", "bound": "hbm",
+    roof = {"kernel": "decode_kernel<192,128,bf16> (balanced ranges)", "bound": "hbm",
             "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
             "frac": dec_gbs / hbm, "peak_kind": pk_kind,
             "traffic": traffic,
@@ -598,7 +608,9 @@ def gpu_arm(args, ws, rank, local):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1), random page placement)",
         "config": {"workload": "batched-decode: 32 seqs, ctx U[2048,8192], q_len 1, "
                    "Hq16/Hkv4, K192/V128, block 16, bf16, 16 splits",
-                   "step": "kv_cache_write(new tokens) + paged_attn_decode + splitkv_reduce",
+                   "segments": "balanced ranges cut on the device (at most 16 per sequence)",
+                   "step": "kv_cache_write(new tokens) + paged_attn_decode_balanced + "
+                           "splitkv_reduce",
                    "l2": "inputs larger than L2 (419 MB KV cache)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roof,

@@ -277,6 +277,57 @@ int pkv_paged_attn_decode(const void *q, int num_q_heads, int num_tokens,
                           float *partial_lse, pkv_stream_t stream);
 
 /*
+ * pkv_paged_attn_decode_balanced -- pkv_paged_attn_decode with the segments
+ * chosen on the device from seq_lens so that every work range carries the
+ * same number of pages (split selection from device-side sequence metadata
+ * under a fixed launch shape, vLLM PR #50371 discussion).
+ *
+ * Segmentation ("balanced ranges"): with P_b = ceil(seq_lens[b] /
+ * block_size), the pages of all sequences are laid end to end in sequence
+ * order (sequence b from global page G_b = P_0 + ... + P_{b-1}, Ptot pages
+ * in all) and cut into ranges of R pages,
+ *   R = max(ceil(Ptot / W), Rmin, 1),  W = num_ranges,
+ *   Rmin = Ptot if max_splits == 1, else floor(max(Pmax - 2, 0) /
+ *          (max_splits - 1)) + 1  (Pmax = max_b P_b),
+ * so that no sequence meets more than max_splits ranges.  Segment s of
+ * sequence b is the part of the sequence inside range floor(G_b / R) + s
+ * (its pages [max(G_b, rR), min(G_b + P_b, (r + 1)R)) - G_b); segments past
+ * the sequence's last range are empty.  partial_o / partial_lse hold
+ * max_splits segments per row and mean what they mean in
+ * pkv_paged_attn_decode (an empty segment: lse -inf, o unwritten), so
+ * pkv_splitkv_reduce(_sink) with num_splits = max_splits merges them.  The
+ * launch runs one CTA per (range, block of KV heads) up to the resident
+ * CTAs of the device and each CTA streams its ranges' pages, so the work is
+ * even whatever the mix of sequence lengths.
+ * num_ranges: W >= 1, or 0 for pkv_decode_balanced_ranges(d) (one
+ * (range, head block) per resident CTA of the current device).  seq_lens[b] <= max_blocks_per_seq
+ * * block_size is required.  Other arguments, layouts and status codes as
+ * in pkv_paged_attn_decode; PKV_EINVAL also for num_ranges < 0 or above
+ * 2^24, or num_seqs * max_blocks_per_seq of 2^31 or more; PKV_EUNSUPPORTED
+ * for more than 128 sequences (use pkv_paged_attn_decode).
+ */
+int pkv_paged_attn_decode_balanced(const void *q, int num_q_heads, int num_tokens,
+                                   const void *cache, const pkv_cache_desc *d,
+                                   const int32_t *block_table, int max_blocks_per_seq,
+                                   const int32_t *seq_lens,
+                                   const int32_t *query_start_loc, int num_seqs,
+                                   int max_query_len, float softmax_scale,
+                                   const float *k_scale, const float *v_scale,
+                                   int max_splits, int num_ranges, float *partial_o,
+                                   float *partial_lse, pkv_stream_t stream);
+
+/*
+ * pkv_decode_balanced_ranges -- the range count W that
+ * pkv_paged_attn_decode_balanced takes for num_ranges = 0 on the current
+ * device: the decode kernel's resident CTAs (SMs x CTAs per SM of the
+ * kernel form that serves this cache) divided by its blocks of KV heads
+ * (the bf16 K192 / V128 form takes four KV heads per block when
+ * num_kv_heads is a multiple of 4, the other forms one), at least 1.
+ * Host-only; a negative status for an invalid or unsupported descriptor.
+ */
+int pkv_decode_balanced_ranges(const pkv_cache_desc *d);
+
+/*
  * pkv_decode_workspace_bytes -- size of the workspace that
  * pkv_paged_attn_decode_fused needs for these sizes: one 32-bit counter per
  * (sequence, KV head, 16-row group of the head's q_len * G rows).  Returns

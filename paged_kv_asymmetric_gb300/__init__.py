@@ -9,7 +9,8 @@ raises.
 
 Functions (same names as the C entry points, without the ``pkv_`` prefix):
 ``kv_cache_write``, ``paged_attn_prefill``, ``paged_attn_decode``,
-``splitkv_reduce``, ``decode_suggest_splits``, ``supports``,
+``paged_attn_decode_balanced``, ``splitkv_reduce``,
+``decode_suggest_splits``, ``decode_balanced_ranges``, ``supports``,
 ``get_device_error``.
 """
 from __future__ import annotations
@@ -37,6 +38,7 @@ EXPORTED = (
     "pkv_decode_workspace_bytes", "pkv_splitkv_reduce", "pkv_splitkv_reduce_sink",
     "pkv_paged_attn_prefill_sink", "pkv_prefill_fp8_workspace_bytes",
     "pkv_paged_attn_prefill_fp8", "pkv_decode_suggest_splits",
+    "pkv_paged_attn_decode_balanced", "pkv_decode_balanced_ranges",
     "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
@@ -100,6 +102,9 @@ def _lib():
                                                     ctypes.c_size_t, P, P, P]
         lib.pkv_paged_attn_decode_fused_noalloc.argtypes = [
             P, I, I, P, D, P, I, P, P, I, I, F, P, P, I, P, P, P, P, P]
+        lib.pkv_paged_attn_decode_balanced.argtypes = [P, I, I, P, D, P, I, P, P, I, I,
+                                                       F, P, P, I, I, P, P, P]
+        lib.pkv_decode_balanced_ranges.argtypes = [D]
         lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_splitkv_reduce.argtypes = [P, P, I, I, I, P, P, P]
@@ -253,6 +258,41 @@ def paged_attn_decode(q, cache: Cache, block_table, seq_lens,
         float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(num_splits),
         _ptr(partial_o), _ptr(partial_lse), _stream(stream)))
     return partial_o, partial_lse
+
+
+def paged_attn_decode_balanced(q, cache: Cache, block_table, seq_lens,
+                               query_start_loc, softmax_scale, max_query_len,
+                               max_splits, num_ranges=0, partial_o=None,
+                               partial_lse=None, k_scale=None, v_scale=None,
+                               stream=None):
+    """Split-KV decode with balanced ranges (pkv_paged_attn_decode_balanced):
+    the segments are cut on the device from seq_lens so that every range of
+    the batch's pages is the same size.  Returns (partial_o [max_splits, T,
+    Hq, dv] f32, partial_lse [max_splits, T, Hq] f32)."""
+    _attn_common(q, block_table, seq_lens, query_start_loc)
+    T, Hq, _ = q.shape
+    dv = cache.desc.head_size_v
+    if partial_o is None:
+        partial_o = torch.empty(max_splits, T, Hq, dv, dtype=torch.float32,
+                                device=q.device)
+    if partial_lse is None:
+        partial_lse = torch.empty(max_splits, T, Hq, dtype=torch.float32,
+                                  device=q.device)
+    _check("pkv_paged_attn_decode_balanced", _lib().pkv_paged_attn_decode_balanced(
+        _ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
+        _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+        _ptr(query_start_loc), int(seq_lens.shape[0]), int(max_query_len),
+        float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(max_splits),
+        int(num_ranges), _ptr(partial_o), _ptr(partial_lse), _stream(stream)))
+    return partial_o, partial_lse
+
+
+def decode_balanced_ranges(cache: Cache) -> int:
+    """The range count pkv_paged_attn_decode_balanced uses for num_ranges=0."""
+    r = _lib().pkv_decode_balanced_ranges(ctypes.byref(cache.desc))
+    if r < 1:
+        raise PkvError("pkv_decode_balanced_ranges", r)
+    return r
 
 
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_query_len) -> int:

@@ -457,6 +457,62 @@ int pkv_paged_attn_decode(const void* q, int num_q_heads, int num_tokens,
   return e == cudaSuccess ? PKV_OK : fail_cuda(e);
 }
 
+namespace {
+
+// One (range, head block) item per resident CTA of the decode kernel.
+int default_ranges(const pkv::AttnParams& p, int sms) {
+  const int slots = pkv::decode_ctas_per_sm(p) * sms;
+  const int hb = pkv::decode_head_blocks(p);
+  return slots / hb > 0 ? slots / hb : 1;
+}
+
+}  // namespace
+
+int pkv_paged_attn_decode_balanced(const void* q, int num_q_heads, int num_tokens,
+                                   const void* cache, const pkv_cache_desc* d,
+                                   const int32_t* block_table, int max_blocks_per_seq,
+                                   const int32_t* seq_lens,
+                                   const int32_t* query_start_loc, int num_seqs,
+                                   int max_query_len, float softmax_scale,
+                                   const float* k_scale, const float* v_scale,
+                                   int max_splits, int num_ranges, float* partial_o,
+                                   float* partial_lse, pkv_stream_t stream) {
+  if (num_ranges < 0 || num_ranges > (1 << 24)) return PKV_EINVAL;
+  // the batch's page line is counted in int
+  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX) return PKV_EINVAL;
+  if (num_seqs > pkv::kBalancedMaxSeqs) return PKV_EUNSUPPORTED;
+  pkv::AttnParams p{};
+  int sms = 0;
+  bool launch = false;
+  const int rc = decode_prepare(q, num_q_heads, num_tokens, cache, d, block_table,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                max_query_len, softmax_scale, k_scale, v_scale, max_splits,
+                                partial_o, partial_lse, &p, &sms, &launch);
+  if (rc != PKV_OK || !launch) return rc;
+  p.split_ranges = num_ranges > 0 ? num_ranges : default_ranges(p, sms);
+  // (range, head block) items are counted in int
+  if (static_cast<int64_t>(p.split_ranges) * pkv::decode_head_blocks(p) > (int64_t{1} << 30))
+    return PKV_EINVAL;
+  cudaError_t e = pkv::launch_decode(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
+  return e == cudaSuccess ? PKV_OK : fail_cuda(e);
+}
+
+int pkv_decode_balanced_ranges(const pkv_cache_desc* d) {
+  int rc = check_desc(d);
+  if (rc != PKV_OK) return rc;
+  if (!pkv::decode_supported(d->head_size, d->head_size_v, d->dtype)) return PKV_EUNSUPPORTED;
+  int sms = 0;
+  rc = device_info(nullptr, &sms);
+  if (rc != PKV_OK) return rc;
+  pkv::AttnParams p{};
+  p.head_size = d->head_size;
+  p.head_size_v = d->head_size_v;
+  p.dtype = d->dtype;
+  p.num_kv_heads = d->num_kv_heads;
+  return default_ranges(p, sms);
+}
+
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                   int max_query_len) {
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_query_len < 1 ||

@@ -134,8 +134,12 @@ struct DecodeCfg {
   // is issued from its page list) never overwrites unit n's.
   static constexpr int ND = NQ > 2 ? NQ : 2;
   static constexpr int MAXSORT = 128;  // sequences ranked by length, at most
+  static_assert(MAXSORT == kBalancedMaxSeqs, "balanced ranges take the ranked batch size");
+  // the sequences' ranking (equal segments) or, for balanced ranges, every
+  // sequence's first global page (MAXSORT + 1 entries, the last = all pages)
   static constexpr int ORDER_OFF = DESC_OFF + ND * DESC_BYTES;
-  static constexpr int MERGE_OFF = ORDER_OFF + MAXSORT * 4;
+  static constexpr int ORDER_BYTES = ((MAXSORT + 1) * 4 + 15) / 16 * 16;
+  static constexpr int MERGE_OFF = ORDER_OFF + ORDER_BYTES;
   // every chunk class's (O, max, sum) per head and row, combined by all
   static constexpr int MROW = DVP + 2;
   static constexpr int MERGE = NG > 1 ? NG * HPC * 16 * MROW * 4 : 0;
@@ -258,27 +262,23 @@ struct UnitShape {
   __device__ int per_seq() const { return S * RG * HB; }
 };
 
-// Unit u's parameters, for sequence b (the rank-u / per_seq sequence) with
-// its query_start_loc pair and length.
+// A unit's parameters from its sequence b (query_start_loc pair q0, q1 and
+// length L), head block, row group, segment s and the segment's pages
+// [page_lo, page_hi) in the sequence's own page numbers.
 template <int KPC>
-__device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, int u, int b,
-                                            int q0, int q1, int L, Unit& un) {
-  const int rem = u % us.per_seq();
-  un.b = b;
-  un.hb = rem % us.HB;
-  const int rg = (rem / us.HB) % us.RG;
-  un.s = rem / (us.HB * us.RG);
+__device__ __forceinline__ void unit_params_pages(const AttnParams& p, int b, int hb, int rg,
+                                                  int s, int q0, int q1, int L, int page_lo,
+                                                  int page_hi, Unit& un) {
   const int G = p.group;
+  un.b = b;
+  un.hb = hb;
+  un.s = s;
   un.qs = q0;
   un.qlen = q1 - q0;
   un.L = L;
   un.row0 = rg * 16;
   un.nrows = max(0, min(16, un.qlen * G - un.row0));
   const int bs = p.block_size;
-  const int P = (un.L + bs - 1) / bs;
-  const int pps = (P + p.num_splits - 1) / p.num_splits;
-  const int page_lo = min(un.s * pps, P);
-  const int page_hi = min(page_lo + pps, P);
   un.klo = page_lo * bs;
   un.khi = min(page_hi * bs, un.L);
   un.kmax = un.klo;
@@ -291,6 +291,24 @@ __device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, i
   un.page_lo = page_lo;
   un.npages = page_hi - page_lo;
   un.pad0 = un.pad1 = 0;
+}
+
+// Unit u's parameters under equal segments, for sequence b (the rank-u /
+// per_seq sequence) with its query_start_loc pair and length: segment s of
+// the sequence's P pages is [s * pps, min((s + 1) * pps, P)), pps =
+// ceil(P / num_splits).
+template <int KPC>
+__device__ __forceinline__ void unit_params(const AttnParams& p, UnitShape us, int u, int b,
+                                            int q0, int q1, int L, Unit& un) {
+  const int rem = u % us.per_seq();
+  const int hb = rem % us.HB;
+  const int rg = (rem / us.HB) % us.RG;
+  const int s = rem / (us.HB * us.RG);
+  const int P = (L + p.block_size - 1) / p.block_size;
+  const int pps = (P + p.num_splits - 1) / p.num_splits;
+  const int page_lo = min(s * pps, P);
+  const int page_hi = min(page_lo + pps, P);
+  unit_params_pages<KPC>(p, b, hb, rg, s, q0, q1, L, page_lo, page_hi, un);
 }
 
 // The end of a unit in the fused decode, run by every consumer thread of
@@ -471,10 +489,111 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
                             : static_cast<int>(blockIdx.x);
       return k * static_cast<int>(gridDim.x) + r;
     };
+    // Balanced ranges (split_ranges = W > 0, at most MAXSORT sequences): the
+    // pages of all sequences laid end to end in sequence order, sequence b
+    // from global page gst[b], cut into ranges of R pages.  A work item is
+    // (range, head block); this CTA takes items blockIdx.x, blockIdx.x +
+    // gridDim.x, ..., and a unit is one (piece of a sequence inside the
+    // item's range, the item's head block, row group).  Items of one range
+    // sit next to each other, so the CTAs that read the different heads of
+    // the same pages run side by side.
+    const bool balanced = p.split_ranges > 0;
+    int* gst = reinterpret_cast<int*>(smem + C::ORDER_OFF);  // [MAXSORT + 1]
+    int64_t bR = 1;     // pages per range
+    int bnr = 0;        // ranges that hold pages
+    if (balanced) {
+      // lane l takes sequences 4l .. 4l + 3: their page counts, then a warp
+      // scan of the lanes' sums gives every sequence's first global page
+      const int nb = p.num_seqs;
+      int P4[4], lsum = 0, lmax = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = 4 * lane + t;
+        const int L = i < nb ? __ldg(p.seq_lens + i) : 0;
+        P4[t] = L > 0 ? (L + bs - 1) / bs : 0;
+        lsum += P4[t];
+        lmax = max(lmax, P4[t]);
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      int g = incl - lsum;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = 4 * lane + t;
+        if (i <= nb) gst[i] = g;
+        g += P4[t];
+      }
+      if (lane == 31 && nb == C::MAXSORT) gst[nb] = g;  // the entry past a full batch
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, d));
+      const int64_t Ptot = __shfl_sync(0xffffffffu, incl, 31);
+      __syncwarp();
+      // R = max(ceil(Ptot / W), Rmin, 1): Rmin keeps every sequence within
+      // num_splits segments (one of P >= 2 pages meets at most
+      // floor((P - 2) / R) + 2 ranges)
+      const int64_t Rmin = p.num_splits == 1 ? Ptot
+                                             : (lmax > 2 ? lmax - 2 : 0) / (p.num_splits - 1) + 1;
+      bR = max(max((Ptot + p.split_ranges - 1) / p.split_ranges, Rmin), int64_t{1});
+      bnr = static_cast<int>((Ptot + bR - 1) / bR);
+      // segments past a sequence's last range hold no key: their lse is
+      // -inf, written here for the sequences b = blockIdx.x (mod gridDim.x)
+      for (int b = blockIdx.x; b < nb; b += gridDim.x) {
+        const int nseg = gst[b + 1] > gst[b]
+                             ? static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1)
+                             : 0;
+        const int q0 = __ldg(p.query_start_loc + b);
+        const int rows = (__ldg(p.query_start_loc + b + 1) - q0) * p.num_q_heads;
+        const int n = (p.num_splits - nseg) * rows;
+        for (int i = lane; i < n; i += 32) {
+          const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
+          p.partial_lse[(static_cast<int64_t>(sg) * T + q0) * p.num_q_heads + rr] = -INFINITY;
+        }
+      }
+    }
+    // work item, sequence, row group of the piece, the piece's pages
+    int bi = blockIdx.x, bb = -1, bj = 0, bplo = 0, bphi = 0;
+    int bL = 0, bq0 = 0, bq1 = 0;  // the piece's sequence: length, query_start_loc pair
+    // moves (bi, bb) to the next piece of a sequence inside the range of one
+    // of this CTA's items; false when there is none
+    auto next_piece = [&]() -> bool {
+      for (;;) {
+        if (bi >= bnr * us.HB) return false;
+        const int64_t r0 = static_cast<int64_t>(bi / us.HB) * bR;
+        const int64_t r1 = r0 + bR;
+        if (bb < 0) {  // the sequence holding global page r0: gst[bb] <= r0 < gst[bb + 1]
+          int lo = 0, hi = p.num_seqs - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (gst[mid + 1] > r0) hi = mid; else lo = mid + 1;
+          }
+          bb = lo;
+        } else {
+          ++bb;
+        }
+        while (bb < p.num_seqs && gst[bb + 1] == gst[bb]) ++bb;  // no pages
+        if (bb < p.num_seqs && gst[bb] < r1) {
+          bplo = static_cast<int>(max(static_cast<int64_t>(gst[bb]), r0) - gst[bb]);
+          bphi = static_cast<int>(min(static_cast<int64_t>(gst[bb + 1]), r1) - gst[bb]);
+          bj = 0;
+          // read here, used when the piece's first unit is built: one unit later
+          bL = __ldg(p.seq_lens + bb);
+          bq0 = __ldg(p.query_start_loc + bb);
+          bq1 = __ldg(p.query_start_loc + bb + 1);
+          return true;
+        }
+        bi += gridDim.x;
+        bb = -1;
+      }
+    };
+    bool bpiece = balanced && next_piece();
     // Sequences ranked by decreasing length (ties by index) when there are
     // few enough to rank here; otherwise in their own order.
     int* order = reinterpret_cast<int*>(smem + C::ORDER_OFF);
-    const bool ranked = p.num_seqs <= C::MAXSORT;
+    const bool ranked = !balanced && p.num_seqs <= C::MAXSORT;
     if (ranked) {
       // lane l holds the lengths of sequences l, l + 32, l + 64, l + 96 and
       // counts, for each, the sequences that come before it
@@ -519,14 +638,32 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         mL = __ldg(p.seq_lens + mb);
       }
     };
-    meta_load(0);
+    if (!balanced) meta_load(0);
+    // the next unit of this CTA's list into `un`; false at the end
+    auto next_unit = [&](Unit& un) -> bool {
+      if (balanced) {
+        if (!bpiece) return false;
+        const int b = bb;
+        unit_params_pages<KPC>(p, b, bi % us.HB, bj,
+                               static_cast<int>(bi / us.HB - gst[b] / bR), bq0, bq1, bL, bplo,
+                               bphi, un);
+        if (++bj == us.RG) bpiece = next_piece();
+        if (un.s >= p.num_splits) {  // excluded by R >= Rmin; never written past the partials
+          set_dev_error(p.err, PKV_EDEV_RANGE);
+          un.nrows = 0;
+        }
+        return true;
+      }
+      if (unit_at(pos) >= num_units) return false;
+      unit_params<KPC>(p, us, unit_at(pos), mb, mq0, mq1, mL, un);
+      ++pos;
+      meta_load(pos);  // the next unit's metadata is in flight meanwhile
+      return true;
+    };
     bool alive = true;
     auto stage_next = [&]() {
-      while (unit_at(pos) < num_units) {
-        Unit un;
-        unit_params<KPC>(p, us, unit_at(pos), mb, mq0, mq1, mL, un);
-        ++pos;
-        meta_load(pos);  // the next unit's metadata is in flight meanwhile
+      Unit un;
+      while (next_unit(un)) {
         if (un.nrows == 0) continue;
         if (un.nch == 0 && !p.fused) {  // no key of this segment is visible to any row
           for (int i = lane; i < HPC * un.nrows; i += 32) {
@@ -1708,8 +1845,12 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                 /*swizzle64=*/true))
     return cudaErrorInvalidValue;
   const int64_t RG = (static_cast<int64_t>(p.max_query_len) * p.group + 15) / 16;
-  const int64_t units = static_cast<int64_t>(p.num_splits) * p.num_seqs *
-                        (p.num_kv_heads / C::HPC) * RG;
+  // equal segments: one CTA per unit up to the resident slots; balanced
+  // ranges: one CTA per (range, head block) up to the resident slots
+  const int64_t units = p.split_ranges > 0
+                            ? static_cast<int64_t>(p.split_ranges) * (p.num_kv_heads / C::HPC)
+                            : static_cast<int64_t>(p.num_splits) * p.num_seqs *
+                                  (p.num_kv_heads / C::HPC) * RG;
   const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
   const int grid = static_cast<int>(units < slots ? units : slots);
   e = launch_pdl(decode_kernel<C>, grid, C::THREADS, C::SMEM, stream, kv_map, kv_map64, p,
@@ -1736,6 +1877,19 @@ using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 2, 1, 576, false, 2>
 using CfgFp8_576 = DecodeCfg<576, 512, true, 1, 4, 1, 64, 4, 2, 576>;
 
 }  // namespace
+
+int decode_ctas_per_sm(const AttnParams& p) {
+  if (p.head_size == 576 && p.head_size_v == 512)
+    return p.dtype == PKV_FP8_E4M3 ? CfgFp8_576::CTAS : CfgBf16_576::CTAS;
+  return 1;
+}
+
+int decode_head_blocks(const AttnParams& p) {
+  // four KV heads per unit only in the bf16 K192 form with Hkv % 4 == 0
+  if (p.head_size == 192 && p.dtype == PKV_BF16 && p.num_kv_heads % 4 == 0)
+    return p.num_kv_heads / 4;
+  return p.num_kv_heads;
+}
 
 bool decode_supported(int head_size, int head_size_v, int dtype) {
   (void)dtype;

@@ -44,8 +44,11 @@ struct AttnParams {
   float softmax_scale;
   const float* k_scale;
   const float* v_scale;
-  // decode
+  // decode: the segment count; with split_ranges = W > 0 the segments are
+  // balanced ranges of the batch's pages (W ranges at most), else equal
+  // shares of each sequence's pages
   int num_splits;
+  int split_ranges;
   float* partial_o;            // [S][T][Hq][dv]
   float* partial_lse;          // [S][T][Hq]
   // prefill, and the fused decode's merged output
@@ -86,6 +89,13 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
 
 // Returns cudaErrorNotSupported for a shape without an instantiation.
 cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream);
+// Resident CTAs per SM of the decode kernel form that serves p's shape, and
+// its head blocks (KV heads / heads per unit).
+int decode_ctas_per_sm(const AttnParams& p);
+int decode_head_blocks(const AttnParams& p);
+// Balanced ranges keep every sequence's first page, length and query range
+// in shared memory: at most this many sequences per launch.
+constexpr int kBalancedMaxSeqs = 128;
 bool decode_supported(int head_size, int head_size_v, int dtype);
 
 // sinks: nullable, one attention-sink logit per query head; row r takes

@@ -153,6 +153,38 @@ def test_valid_shapes_pass_the_host_checks(lib):
     assert _fused(lib, bf, T=32, B=32, mb=512, S=16) == pkv.ECUDA
 
 
+def _balanced(lib, d, W=0, **kw):
+    a = dict(q=DUMMY, Hq=16, T=4, cache=DUMMY, bt=DUMMY, mb=4, sl=DUMMY, qsl=DUMMY,
+             B=1, mq=1, scale=0.1, ks=None, vs=None, S=4, po=DUMMY, pl=DUMMY)
+    a.update(kw)
+    return lib.pkv_paged_attn_decode_balanced(
+        a["q"], a["Hq"], a["T"], a["cache"], ctypes.byref(d), a["bt"], a["mb"], a["sl"],
+        a["qsl"], a["B"], a["mq"], ctypes.c_float(a["scale"]), a["ks"], a["vs"], a["S"],
+        W, a["po"], a["pl"], None)
+
+
+def test_balanced_decode_rejects_bad_arguments(lib):
+    d = _desc()
+    assert _balanced(lib, d, W=-1) == pkv.EINVAL
+    assert _balanced(lib, d, W=(1 << 24) + 1) == pkv.EINVAL
+    assert _balanced(lib, d, B=129) == pkv.EUNSUPPORTED      # more than 128 sequences
+    assert _balanced(lib, d, B=64, mb=1 << 26) == pkv.EINVAL  # page line past int
+    assert _balanced(lib, d, S=0) == pkv.EINVAL
+    assert _balanced(lib, d, po=None) == pkv.EINVAL
+    assert _balanced(lib, d, T=0) == pkv.OK
+    assert lib.pkv_decode_balanced_ranges(None) == pkv.EINVAL
+    assert lib.pkv_decode_balanced_ranges(ctypes.byref(_desc(
+        head_size=64, head_size_v=64, row_elems=128, v_off=64))) == pkv.EUNSUPPORTED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(),
+                    reason="a valid call would launch on the dummy pointers")
+def test_balanced_shapes_pass_the_host_checks(lib):
+    bf = _desc(num_blocks=4096)
+    assert _balanced(lib, bf, T=32, B=32, mb=512, S=16) == pkv.ECUDA
+    assert _balanced(lib, bf, W=152, T=128, B=128, mb=512, S=16) == pkv.ECUDA
+
+
 def test_prefill_rejects_bad_arguments(lib):
     def call(d, **kw):
         a = dict(q=DUMMY, Hq=16, T=4, scale=0.1, out=DUMMY)

@@ -1,0 +1,130 @@
+"""Split-KV decode with balanced ranges (pkv_paged_attn_decode_balanced) on
+the GPU against the oracle: the segments the device cuts from seq_lens are
+the oracle's balanced ranges for the same W, partial by partial (lse within
+2e-3 / 1e-4, o within the path's tolerance: bf16 1e-2 / 1e-2, FP8 KV 3e-2),
+and the merged rows equal whole-row attention."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_asymmetric_gb300 as pkv
+from paged_kv_asymmetric_gb300 import workloads as wl
+from tests import gpu_path, refs
+from tests.test_decode_gpu import SMALL, _check_out
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(dw, S, W):
+    w = dw.w
+    po, pl = pkv.paged_attn_decode_balanced(
+        dw.q, dw.cache, dw.block_table, dw.seq_lens, dw.query_start_loc,
+        w.softmax_scale, max(1, w.max_query_len), S, W,
+        k_scale=dw.k_scale, v_scale=dw.v_scale)
+    lse = torch.empty(pl.shape[1:], dtype=torch.float32, device=pl.device)
+    out = pkv.splitkv_reduce(po, pl, lse_out=lse)
+    torch.cuda.synchronize()
+    return po, pl, out, lse
+
+
+def _check_partials(w, po, pl, S, W, tokens=None, seqs=None, splits=None):
+    sel = slice(None) if tokens is None else torch.from_numpy(
+        np.asarray(tokens, dtype=np.int64)).cuda()
+    po, pl = po[:, sel], pl[:, sel]
+    for s in (range(S) if splits is None else splits):
+        o, l = gpu_path.oracle_rows(w, tokens=tokens, seqs=seqs, num_splits=S,
+                                    split=s, split_ranges=W)
+        gl = gpu_path.host(pl[s])
+        fin = np.isfinite(l)
+        assert (np.isneginf(gl) == ~fin).all(), f"segment {s}: empty pattern"
+        assert not np.isnan(gl).any()
+        refs.assert_close(gl[fin], l[fin], atol=2e-3, rtol=1e-4, what=f"lse {s}")
+        go = gpu_path.host(po[s])
+        refs.assert_close(go[fin], o[fin], **gpu_path.tol(w), what=f"o {s}")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("S,W", [(1, 0), (4, 3), (8, 0), (16, 7), (16, 1000)])
+def test_balanced_small(name, S, W):
+    w = SMALL[name]()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    We = W or pkv.decode_balanced_ranges(dw.cache)
+    po, pl, out, lse = _decode(dw, S, W)
+    _check_partials(w, po, pl, S, We)
+    _check_out(w, out, lse)
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_mixed_lengths_and_empty_sequences():
+    """One long sequence among short and empty ones: the ranges cut the long
+    one into many segments and leave the padded rows at -inf everywhere."""
+    w = wl.make_workload("mix", seq_lens=[5000, 3, 0, 40, 0, 700, 17],
+                         q_lens=[1, 1, 4, 2, 1, 4, 1], block_size=16, seed=21)
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    for S, W in ((16, 0), (32, 5), (3, 152)):
+        We = W or pkv.decode_balanced_ranges(dw.cache)
+        po, pl, out, lse = _decode(dw, S, W)
+        _check_partials(w, po, pl, S, We)
+        _check_out(w, out, lse)
+        empty = gpu_path.tokens_of(w, [2, 4])
+        assert np.isneginf(gpu_path.host(pl)[:, empty]).all()
+        assert (gpu_path.host(out)[empty] == 0).all()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_repeatable_and_many_ranges_per_cta():
+    """Two calls give the same bits; W above the resident CTAs (so a CTA
+    takes several ranges) matches the oracle."""
+    w = SMALL["verify-bf16"]()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    W = 3 * pkv.decode_balanced_ranges(dw.cache)
+    a = [t.clone() for t in _decode(dw, 64, W)]
+    b = _decode(dw, 64, W)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    written = torch.isfinite(b[1])   # an empty segment's o is left unwritten
+    assert torch.equal(a[0][written], b[0][written])
+    _check_partials(w, b[0], b[1], 64, W)
+
+
+def test_balanced_rejects_large_batches():
+    w = wl.make_workload("many", seq_lens=[20] * 129, q_lens=[1] * 129, seed=22)
+    dw = wl.to_device(w)
+    with pytest.raises(pkv.PkvError) as e:
+        _decode(dw, 4, 0)
+    assert e.value.status == pkv.EUNSUPPORTED
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_attn_decode_balanced(
+            dw.q, dw.cache, dw.block_table, dw.seq_lens, dw.query_start_loc,
+            w.softmax_scale, 1, 4, -1)
+    assert e.value.status == pkv.EINVAL
+
+
+# ----------------------------------------------------------- full sizes ----
+
+def test_balanced_batched_decode_full():
+    """The batched-decode workload in the bench's launch shape (16 segments
+    at most, one range per resident CTA): every merged row, and the
+    partials of every sequence for four of the segments."""
+    w = wl.batched_decode()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    W = pkv.decode_balanced_ranges(dw.cache)
+    po, pl, out, lse = _decode(dw, w.max_splits, W)
+    _check_out(w, out, lse)
+    _check_partials(w, po, pl, w.max_splits, W, splits=[0, 1, 4, 15])
+
+
+def test_balanced_verify_fp8_full():
+    """16 x ~46K keys, q_len 4, FP8 per-head scales, block 64, 8 padded
+    rows: every row of every sequence."""
+    w = wl.verify_fp8()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    _, pl, out, lse = _decode(dw, 16, 0)
+    _check_out(w, out, lse)
+    assert np.isneginf(gpu_path.host(pl)[:, 64:]).all()

@@ -167,18 +167,28 @@ def test_batched_decode_full():
     _check_out(w, out, lse)
 
 
-def test_verify_fp8_full_sampled():
+def test_verify_fp8_full():
     """16 x ~46K keys, q_len 4, FP8 per-head scales, block 64, 16 splits,
-    8 padded rows: every row of three sequences and of the padded ones."""
+    8 padded rows: every row of every sequence, and the partials of three
+    segments."""
     w = wl.verify_fp8()
     dw = wl.to_device(w)
     gpu_path.write_all(dw)
-    _, _, out, lse = gpu_path.decode(dw, 16)
-    seqs = [0, 7, 15]
-    toks = gpu_path.tokens_of(w, seqs)
-    _check_out(w, out, lse, tokens=toks, seqs=seqs)
+    po, pl, out, lse = gpu_path.decode(dw, 16)
+    _check_out(w, out, lse)
     o = gpu_path.host(out)
     assert (o[64:] == 0).all() and np.isfinite(o).all()
+    seqs = [0, 15]
+    toks = gpu_path.tokens_of(w, seqs)
+    sel = torch.from_numpy(toks.astype(np.int64)).cuda()
+    for s in (0, 7, 15):
+        o_s, l_s = gpu_path.oracle_rows(w, tokens=toks, seqs=seqs, num_splits=16, split=s)
+        gl = gpu_path.host(pl[s, sel])
+        fin = np.isfinite(l_s)
+        assert (np.isneginf(gl) == ~fin).all()
+        refs.assert_close(gl[fin], l_s[fin], atol=2e-3, rtol=1e-4, what=f"lse split {s}")
+        refs.assert_close(gpu_path.host(po[s, sel])[fin], o_s[fin], **gpu_path.FP8_TOL,
+                          what=f"partial o split {s}")
 
 
 @pytest.mark.parametrize("heads", [12, 16])
@@ -191,13 +201,14 @@ def test_mla_full_b1(heads):
     _check_out(w, out, lse)
 
 
-def test_mla_full_b16_sampled():
+def test_mla_full_b16():
+    """Batch 16 at 100K context, 16 heads (12 real + 4 zero): every row."""
     w = wl.mla_decode(batch=16, heads=16)
     dw = wl.to_device(w)
     gpu_path.write_all(dw)
     S = pkv.decode_suggest_splits(16, 16, 1, 1, 100000, 64)
     _, _, out, lse = gpu_path.decode(dw, S)
-    _check_out(w, out, lse, tokens=np.array([0, 9], np.int32), seqs=[0, 9])
+    _check_out(w, out, lse)
 
 
 def test_out_of_range_page_is_reported():

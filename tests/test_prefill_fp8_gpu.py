@@ -91,10 +91,13 @@ def test_fp8_prefill_repeatable_and_workspace_checks():
 
 def test_fp8_prefill_32k_sampled():
     """32,768 tokens, FP8 cache with per-head scales, in the bench's launch
-    shape; sampled rows, every head, against the oracle."""
+    shape: the tokens of the bf16 32K test's choice (first and last dealt
+    units, both CTAs and both tiles of each, tile edges) and a random
+    spread, every head, against the oracle."""
+    from tests.test_prefill_gpu import prefill_sample_tokens
     w = wl.make_workload("prefill-32768-fp8", seq_lens=[32768], q_lens=[32768],
                          kv_dtype=wl.FP8, scale_mode=H, seed=0)
-    rng = np.random.default_rng(1)
-    toks = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 32767],
-                                     rng.integers(0, 32768, 8)])).astype(np.int32)
+    units = [0, 1, 2, 8, 9, 63, 64, 100, 127, 128, 200, 236, 237, 254, 255]
+    toks = prefill_sample_tokens(32768, units, 24, seed=1)
+    assert len(toks) * 16 >= 2048
     _run(w, tokens=toks, seqs=[0])

@@ -83,15 +83,60 @@ def test_prefill_repeatable():
     assert torch.equal(a, b)
 
 
+def prefill_sample_tokens(n_tokens, units, n_random, seed=0, G=4, kv_heads=4):
+    """Query tokens to check in a long single-sequence prefill, chosen from
+    the kernel's work numbering: a query tile is 128 / G tokens of the G
+    query heads of one KV head; unit u of a KV head holds tiles 4u .. 4u + 3
+    (tiles 4u, 4u + 1 -- a work item's tiles A and B -- go to the first CTA
+    of a 2-CTA cluster, 4u + 2 and 4u + 3 to the second); units are numbered
+    from the last (longest) one and dealt to the clusters in rounds.  For
+    each listed unit the first and last token of each of its four tiles is
+    taken (every query head of those tokens is compared, so every KV head's
+    unit is covered), plus the first and last token of the sequence and a
+    random spread."""
+    tq = 128 // G
+    toks = [0, n_tokens - 1]
+    for u in units:
+        for tile in range(4):
+            t0 = (4 * u + tile) * tq
+            toks += [t0, t0 + tq - 1]
+    rng = np.random.default_rng(seed)
+    toks += list(rng.integers(0, n_tokens, n_random))
+    return np.unique(np.asarray(toks, dtype=np.int64)).astype(np.int32)
+
+
+def _long_prefill_check(n_tokens, units, n_random):
+    w = wl.long_prefill(n_tokens)
+    toks = prefill_sample_tokens(n_tokens, units, n_random)
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    gpu_path.device_error()
+    out = gpu_path.prefill(dw)
+    got = gpu_path.host(out[torch.from_numpy(toks.astype(np.int64)).cuda()])
+    torch.cuda.synchronize()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+    o, _ = gpu_path.oracle_rows(w, tokens=toks, seqs=[0])
+    refs.assert_close(got, o, **gpu_path.BF16_TOL, what=w.name)
+    return toks
+
+
 def test_prefill_32k_sampled():
     """The long-prefill workload: 32,768 tokens, causal, in the bench's launch
-    shape; rows checked against the oracle: the first, the last, and a spread
-    between them, every head."""
-    w = wl.long_prefill(32768)
-    rng = np.random.default_rng(0)
-    toks = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 32767],
-                                     rng.integers(0, 32768, 10)])).astype(np.int32)
-    _run_and_check(w, tokens=toks, seqs=[0])
+    shape.  1,024 tiles of 32 tokens make 256 units per KV head (1,024 in
+    all, 76 clusters on 152 SMs): the units dealt first (255 .. 237), last
+    (0 .. 8) and between, both CTAs and both tiles of each, every head."""
+    units = [0, 1, 2, 8, 9, 63, 64, 100, 127, 128, 200, 236, 237, 254, 255]
+    toks = _long_prefill_check(32768, units, 24)
+    assert len(toks) * 16 >= 2048
+
+
+def test_prefill_131k_sampled():
+    """The 131,072-token prefill (the long-prefill workload's larger run):
+    4,096 units per KV head; the first and last dealt units, the middle
+    ones, tile edges and a random spread, every head."""
+    units = [0, 1, 2, 511, 512, 1000, 1021, 1022, 1023]
+    toks = _long_prefill_check(131072, units, 16)
+    assert len(toks) * 16 >= 1024
 
 
 def _raw_prefill(q_ptr, cache_ptr, out_ptr, dw):
