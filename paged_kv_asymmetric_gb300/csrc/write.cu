@@ -159,9 +159,23 @@ __global__ void __launch_bounds__(256)
 // the vector path, but with each lane's piece geometry (source and
 // destination offsets, K or V, scale) computed once for all tokens, which
 // takes at most 32 * PPL pieces per token.  A token's loads do not wait for
-// its slot: they are issued first, and the slot decides the stores.
+// its slot: they are issued first, and the slot decides the stores.  A warp
+// that has more than one token (grid-stride) loads its next token's pieces
+// and slot before it encodes and stores the current one, so the FP8 encode
+// of one token overlaps the loads of the next.
+// Loads of the next token are kept in registers beside the current ones
+// (WR_PREFETCH) when a lane's pieces are at most 8 16-byte loads; the block
+// count per SM is then the one whose register share holds both sets.
 template <bool FP8, int EPT, int PPL>
-__global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 : 8)) ? 3 : 1)
+constexpr bool WR_PREFETCH = PPL * (EPT / 8) <= 8;
+template <bool FP8, int EPT, int PPL>
+constexpr int WR_BLOCKS =
+    WR_PREFETCH<FP8, EPT, PPL>
+        ? (PPL * (EPT / 8) <= (FP8 ? 4 : 5) ? 3 : 2)
+        : ((FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 : 8)) ? 3 : 1);
+
+template <bool FP8, int EPT, int PPL>
+__global__ void __launch_bounds__(256, (WR_BLOCKS<FP8, EPT, PPL>))
     cache_write_tok_kernel(WriteParams p) {
   pdl_trigger();  // the next kernel of the step may start launching
   pdl_wait();     // every global access comes after the kernel ahead completes
@@ -203,12 +217,11 @@ __global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 
     }
   }
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       t < p.num_tokens; t += warps) {
-    const int64_t slot = __ldg(p.slot_mapping + t);
+  // token t's slot and pieces, loaded into (slot, v)
+  auto load = [&](int64_t t, int64_t& slot, uint4 (&v)[PPL][NV]) {
+    slot = __ldg(p.slot_mapping + t);
     const __nv_bfloat16* kt = p.key + t * p.key_tok_stride;
     const __nv_bfloat16* vt = p.has_value ? p.value + t * p.val_tok_stride : kt;
-    uint4 v[PPL][NV];
 #pragma unroll
     for (int j = 0; j < PPL; ++j)
       if (act[j]) {
@@ -216,6 +229,26 @@ __global__ void __launch_bounds__(256, (FP8 && PPL <= 3) ? 4 : (PPL <= (FP8 ? 4 
 #pragma unroll
         for (int c = 0; c < NV; ++c) v[j][c] = __ldg(src + c);
       }
+  };
+  constexpr bool kPrefetch = WR_PREFETCH<FP8, EPT, PPL>;
+  int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  int64_t next_slot = -1;
+  uint4 nv[kPrefetch ? PPL : 1][NV];
+  if (kPrefetch && t < p.num_tokens) load(t, next_slot, *reinterpret_cast<uint4(*)[PPL][NV]>(nv));
+  for (; t < p.num_tokens; t += warps) {
+    int64_t slot;
+    uint4 v[PPL][NV];
+    if constexpr (kPrefetch) {
+      slot = next_slot;
+#pragma unroll
+      for (int j = 0; j < PPL; ++j)
+#pragma unroll
+        for (int c = 0; c < NV; ++c) v[j][c] = nv[j][c];
+      if (t + warps < p.num_tokens)
+        load(t + warps, next_slot, *reinterpret_cast<uint4(*)[PPL][NV]>(nv));
+    } else {
+      load(t, slot, v);
+    }
     if (slot < 0) continue;
     if (slot >= nslots) {
       if (lane == 0) set_dev_error(p.err, PKV_EDEV_RANGE);
@@ -301,6 +334,20 @@ inline bool aligned(const void* p, int bytes) {
   return (reinterpret_cast<uintptr_t>(p) % bytes) == 0;
 }
 
+// The token path's launch: one warp per token (8 per block) when a warp
+// keeps one token in registers; with the next token's loads kept as well,
+// the resident blocks only (WR_BLOCKS per SM), each warp striding over
+// tokens so that its loads run one token ahead.
+template <bool FP8, int EPT, int PPL>
+cudaError_t launch_tok(const WriteParams& p, int num_sms, cudaStream_t stream) {
+  const int64_t blocks = (static_cast<int64_t>(p.num_tokens) + 7) / 8;
+  int64_t cap = int64_t{1} << 30;
+  if (WR_PREFETCH<FP8, EPT, PPL>) cap = static_cast<int64_t>(num_sms) * WR_BLOCKS<FP8, EPT, PPL>;
+  const unsigned grid =
+      static_cast<unsigned>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  return launch_pdl(cache_write_tok_kernel<FP8, EPT, PPL>, grid, 256, 0, stream, p);
+}
+
 }  // namespace
 
 cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
@@ -339,9 +386,6 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
   const int ept = fp8 ? (vec_ok(16) ? 16 : 8) : 8;
   const int pieces = p.num_kv_heads * (p.head_size / ept +
                                        (p.has_value ? p.head_size_v / ept : 0));
-  const int64_t tblocks64 = (static_cast<int64_t>(p.num_tokens) + 7) / 8;
-  const unsigned tgrid = static_cast<unsigned>(
-      tblocks64 < (int64_t{1} << 30) ? (tblocks64 > 0 ? tblocks64 : 1) : (int64_t{1} << 30));
   // the token path keeps per-lane offsets in 32 bits: a token's K / V rows
   // and a slot's rows of all heads must span less than 2^31 elements
   const int64_t src_span = static_cast<int64_t>(p.num_kv_heads) *
@@ -353,19 +397,19 @@ cudaError_t launch_cache_write(const WriteParams& p, int num_sms,
   cudaError_t e = cudaSuccess;
   if (tok) {
     if (!fp8) {
-      if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<false, 8, 4>, tgrid, threads, 0, stream, p);
-      else if (pieces <= 160) e = launch_pdl(cache_write_tok_kernel<false, 8, 5>, tgrid, threads, 0, stream, p);
-      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<false, 8, 8>, tgrid, threads, 0, stream, p);
-      else e = launch_pdl(cache_write_tok_kernel<false, 8, 16>, tgrid, threads, 0, stream, p);
+      if (pieces <= 128) e = launch_tok<false, 8, 4>(p, num_sms, stream);
+      else if (pieces <= 160) e = launch_tok<false, 8, 5>(p, num_sms, stream);
+      else if (pieces <= 256) e = launch_tok<false, 8, 8>(p, num_sms, stream);
+      else e = launch_tok<false, 8, 16>(p, num_sms, stream);
     } else if (ept == 16) {
-      if (pieces <= 96) e = launch_pdl(cache_write_tok_kernel<true, 16, 3>, tgrid, threads, 0, stream, p);
-      else if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<true, 16, 4>, tgrid, threads, 0, stream, p);
-      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<true, 16, 8>, tgrid, threads, 0, stream, p);
-      else e = launch_pdl(cache_write_tok_kernel<true, 16, 16>, tgrid, threads, 0, stream, p);
+      if (pieces <= 96) e = launch_tok<true, 16, 3>(p, num_sms, stream);
+      else if (pieces <= 128) e = launch_tok<true, 16, 4>(p, num_sms, stream);
+      else if (pieces <= 256) e = launch_tok<true, 16, 8>(p, num_sms, stream);
+      else e = launch_tok<true, 16, 16>(p, num_sms, stream);
     } else {
-      if (pieces <= 128) e = launch_pdl(cache_write_tok_kernel<true, 8, 4>, tgrid, threads, 0, stream, p);
-      else if (pieces <= 256) e = launch_pdl(cache_write_tok_kernel<true, 8, 8>, tgrid, threads, 0, stream, p);
-      else e = launch_pdl(cache_write_tok_kernel<true, 8, 16>, tgrid, threads, 0, stream, p);
+      if (pieces <= 128) e = launch_tok<true, 8, 4>(p, num_sms, stream);
+      else if (pieces <= 256) e = launch_tok<true, 8, 8>(p, num_sms, stream);
+      else e = launch_tok<true, 8, 16>(p, num_sms, stream);
     }
   } else if (!fp8 && vec_ok(8)) {
     e = launch_pdl(cache_write_vec_kernel<false, 8>, vgrid, threads, 0, stream, p);

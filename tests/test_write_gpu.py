@@ -138,3 +138,24 @@ def test_out_of_range_slot_is_skipped_and_reported():
     slots2[5] = -1
     exp = _oracle_bytes(w, slots2)
     assert (got[dw.slack:-dw.slack] == exp).all()
+
+
+@pytest.mark.parametrize("kv", [(wl.BF16, wl.SCALE_NONE), (wl.FP8, wl.SCALE_HEAD),
+                                (wl.FP8, wl.SCALE_TENSOR)])
+def test_write_many_tokens_per_warp(kv):
+    """More tokens than the launch has warps, so each warp strides over
+    several tokens and loads the next one while it stores the current one;
+    skipped (negative) slots sit among them.  Bit-exact with the oracle."""
+    T = 20011
+    w, slots = _case(wl.NHD, kv[0], kv[1], 16, T, seed=3)
+    slots = slots.copy()
+    slots[::7] = -1
+    dw = wl.to_device(w)
+    s = torch.from_numpy(slots).cuda()
+    pkv.kv_cache_write(dw.k_ctx, dw.v_ctx, s, dw.cache, dw.k_scale, dw.v_scale)
+    got = dw.cache_buf.cpu().numpy()
+    exp = _oracle_bytes(w, slots)
+    assert (got[:dw.slack] == 0xFF).all() and (got[-dw.slack:] == 0xFF).all()
+    bad = np.nonzero(got[dw.slack:-dw.slack] != exp)[0]
+    assert bad.size == 0, f"{bad.size} bytes differ, first at {bad[:8]}"
+    assert gpu_path.device_error() == pkv.EDEV_NONE
