@@ -396,7 +396,10 @@ __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un
   named_barrier(1, NT);  // the weights are read before the buffer is reused
 }
 
-template <class C>
+// BAL: the balanced-range unit list (split_ranges > 0) is compiled in; the
+// equal-segment form is its own instantiation, so that the code of one list
+// does not weigh on the other's register allocation.
+template <class C, bool BAL>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map,
                   const __grid_constant__ CUtensorMap kv_map64, const AttnParams p,
@@ -497,19 +500,43 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     // item's range, the item's head block, row group).  Items of one range
     // sit next to each other, so the CTAs that read the different heads of
     // the same pages run side by side.
-    const bool balanced = p.split_ranges > 0;
+    constexpr bool balanced = BAL;
     int* gst = reinterpret_cast<int*>(smem + C::ORDER_OFF);  // [MAXSORT + 1]
+    // query_start_loc[b] and seq_lens[b] of the lane registers (b uniform
+    // over the warp; b == num_seqs gives the last query_start_loc entry)
+    int L4_[4], Q4_[4], qend_ = 0;
+    auto pick4 = [&](const int (&a)[4], int b) {
+      const int t = b & 3;
+      const int v = t == 0 ? a[0] : t == 1 ? a[1] : t == 2 ? a[2] : a[3];
+      return __shfl_sync(0xffffffffu, v, (b >> 2) & 31);
+    };
+    auto seq_q = [&](int b) { return b >= p.num_seqs ? qend_ : pick4(Q4_, b); };
+    auto seq_L = [&](int b) { return pick4(L4_, b); };
     int64_t bR = 1;     // pages per range
     int bnr = 0;        // ranges that hold pages
+    // lane l holds the lengths and first query tokens of sequences 4l ..
+    // 4l + 3 (balanced ranges), read with the lengths, so that no later
+    // metadata read stands between the lengths and the first copy
+    int (&L4)[4] = L4_;
+    int (&Q4)[4] = Q4_;
+    int& qend = qend_;
+    L4[0] = L4[1] = L4[2] = L4[3] = 0;
+    Q4[0] = Q4[1] = Q4[2] = Q4[3] = 0;
     if (balanced) {
       // lane l takes sequences 4l .. 4l + 3: their page counts, then a warp
       // scan of the lanes' sums gives every sequence's first global page
       const int nb = p.num_seqs;
       int P4[4], lsum = 0, lmax = 0;
+      qend = __ldg(p.query_start_loc + nb);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int i = 4 * lane + t;
-        const int L = i < nb ? __ldg(p.seq_lens + i) : 0;
+        L4[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+        Q4[t] = i < nb ? __ldg(p.query_start_loc + i) : 0;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int L = L4[t];
         P4[t] = L > 0 ? (L + bs - 1) / bs : 0;
         lsum += P4[t];
         lmax = max(lmax, P4[t]);
@@ -545,8 +572,8 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         const int nseg = gst[b + 1] > gst[b]
                              ? static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1)
                              : 0;
-        const int q0 = __ldg(p.query_start_loc + b);
-        const int rows = (__ldg(p.query_start_loc + b + 1) - q0) * p.num_q_heads;
+        const int q0 = seq_q(b);
+        const int rows = (seq_q(b + 1) - q0) * p.num_q_heads;
         const int n = (p.num_splits - nseg) * rows;
         for (int i = lane; i < n; i += 32) {
           const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
@@ -579,10 +606,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           bplo = static_cast<int>(max(static_cast<int64_t>(gst[bb]), r0) - gst[bb]);
           bphi = static_cast<int>(min(static_cast<int64_t>(gst[bb + 1]), r1) - gst[bb]);
           bj = 0;
-          // read here, used when the piece's first unit is built: one unit later
-          bL = __ldg(p.seq_lens + bb);
-          bq0 = __ldg(p.query_start_loc + bb);
-          bq1 = __ldg(p.query_start_loc + bb + 1);
+          bL = seq_L(bb);
+          bq0 = seq_q(bb);
+          bq1 = seq_q(bb + 1);
           return true;
         }
         bi += gridDim.x;
@@ -600,10 +626,16 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
       static_assert(C::MAXSORT == 128, "four sequences per lane");
       const int nb = p.num_seqs, nu = (nb + 31) / 32;
       int v[4], rank[4];
+      // the query_start_loc entries come with the lengths (lane l: sequences
+      // l, l + 32, l + 64, l + 96, and the last entry), so that the first
+      // unit's metadata needs no read of its own
+      qend_ = __ldg(p.query_start_loc + nb);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int i = lane + 32 * t;
         v[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+        Q4_[t] = i < nb ? __ldg(p.query_start_loc + i) : 0;
+        L4_[t] = v[t];
         rank[t] = 0;
       }
       for (int u = 0; u < nu; ++u) {
@@ -629,13 +661,26 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     };
     int pos = 0;                   // next position in this CTA's unit list
     int mb = 0, mq0 = 0, mq1 = 0, mL = 0;  // metadata of the unit at `pos`
+    // sequence b's entry of a ranked batch's lane registers (lane b % 32,
+    // register b / 32; b uniform over the warp)
+    auto pick32 = [&](const int (&a)[4], int b) {
+      const int t = (b >> 5) & 3;
+      const int x = t == 0 ? a[0] : t == 1 ? a[1] : t == 2 ? a[2] : a[3];
+      return __shfl_sync(0xffffffffu, x, b & 31);
+    };
     auto meta_load = [&](int ps) {
       const int u = unit_at(ps);
       if (u < num_units) {
         mb = seq_of(u);
-        mq0 = __ldg(p.query_start_loc + mb);
-        mq1 = __ldg(p.query_start_loc + mb + 1);
-        mL = __ldg(p.seq_lens + mb);
+        if (ranked) {
+          mq0 = pick32(Q4_, mb);
+          mq1 = mb + 1 < p.num_seqs ? pick32(Q4_, mb + 1) : qend_;
+          mL = pick32(L4_, mb);
+        } else {
+          mq0 = __ldg(p.query_start_loc + mb);
+          mq1 = __ldg(p.query_start_loc + mb + 1);
+          mL = __ldg(p.seq_lens + mb);
+        }
       }
     };
     if (!balanced) meta_load(0);
@@ -1821,8 +1866,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
 
 template <class C>
 cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
-  static int attr_set[64] = {0};
-  cudaError_t e = ensure_smem_attr(decode_kernel<C>, C::SMEM, attr_set);
+  static int attr_set[2][64] = {{0}};
+  const bool bal = p.split_ranges > 0;
+  cudaError_t e = bal ? ensure_smem_attr(decode_kernel<C, true>, C::SMEM, attr_set[1])
+                      : ensure_smem_attr(decode_kernel<C, false>, C::SMEM, attr_set[0]);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap kv_map;
   const int box_rows = box_rows_for(p.block_size, C::KPC);
@@ -1853,8 +1900,10 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                   (p.num_kv_heads / C::HPC) * RG;
   const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
   const int grid = static_cast<int>(units < slots ? units : slots);
-  e = launch_pdl(decode_kernel<C>, grid, C::THREADS, C::SMEM, stream, kv_map, kv_map64, p,
-                 head_boxes);
+  e = bal ? launch_pdl(decode_kernel<C, true>, grid, C::THREADS, C::SMEM, stream, kv_map,
+                       kv_map64, p, head_boxes)
+          : launch_pdl(decode_kernel<C, false>, grid, C::THREADS, C::SMEM, stream, kv_map,
+                       kv_map64, p, head_boxes);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
