@@ -381,7 +381,7 @@ def gpu_arm(args, ws, rank, local):
 
     def prefill_fp8_sub(name, n_tokens):
         # the same causal prefill over an FP8 E4M3 cache (per-head scales):
-        # the whole public call, the widening pass included
+        # the codes are widened in the kernel, no workspace
         require_single_gpu(ws, name)
         wk = wl.make_workload(f"prefill-{n_tokens}-fp8", seq_lens=[n_tokens],
                               q_lens=[n_tokens], kv_dtype=wl.FP8,
@@ -391,21 +391,26 @@ def gpu_arm(args, ws, rank, local):
                            dwk.k_scale, dwk.v_scale)
         outk = torch.empty(wk.num_tokens, wk.num_q_heads, wk.head_size_v,
                            dtype=torch.bfloat16, device=dev)
-        nws = pkv.prefill_fp8_workspace_bytes(wk.num_seqs, dwk.block_table.shape[1],
-                                              dwk.cache)
-        wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
 
-        def pf8():
+        def pf8(ws=None):
             pkv.paged_attn_prefill(dwk.q, dwk.cache, dwk.block_table,
                                    dwk.seq_lens, dwk.query_start_loc,
                                    wk.softmax_scale, out=outk, k_scale=dwk.k_scale,
-                                   v_scale=dwk.v_scale, workspace=wsp)
+                                   v_scale=dwk.v_scale, workspace=ws)
         mp, _ = time_launches(pf8, reps, 2, flush)
+        # the two-pass form: pages widened into a workspace, then the prefill
+        nws = pkv.prefill_fp8_workspace_bytes(wk.num_seqs, dwk.block_table.shape[1],
+                                              dwk.cache)
+        wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
+        m2, _ = time_launches(lambda: pf8(wsp), reps, 2, flush)
         fl = prefill_flops(wk)
         sub[name] = {"prefill_ms": mp, "tflop": fl / 1e12,
                      "TFLOPs": fl / (mp * 1e-3) / 1e12,
                      "frac_bf16": fl / (mp * 1e-3) / 1e12 / tf_burst,
-                     "workspace_bytes": nws}
+                     "form": "E4M3 widened in the kernel, no workspace",
+                     "two_pass_ms": m2, "two_pass_TFLOPs": fl / (m2 * 1e-3) / 1e12,
+                     "two_pass_frac_bf16": fl / (m2 * 1e-3) / 1e12 / tf_burst,
+                     "two_pass_workspace_bytes": nws}
         del dwk, outk, wsp
         torch.cuda.empty_cache()
 

@@ -155,11 +155,19 @@ int pkv_kv_cache_write(const void *key, int64_t key_tok_stride,
  * sees none is written as 0.  The K and V of every visible key must already
  * be in the cache.  Keys past seq_lens[b] in the last page are never used,
  * whatever the cache holds there.
- * softmax_scale must be > 0.  k_scale / v_scale as in the write (fp8
- * caches; NULL for bf16).
- * This build: bf16 cache, head_size 192 and head_size_v 128, num_q_heads /
- * num_kv_heads dividing 128, block_size a power of two >= 8, K at a
- * 64-element column offset; otherwise PKV_EUNSUPPORTED.  PKV_EINVAL for null
+ * softmax_scale must be > 0.
+ * FP8 E4M3 cache (the MiMo model card's production setting, "What the
+ * kernels do": FP8 K/V converted in the kernel, Q.K^T kept in 16-bit, its
+ * FP8 Q.K^T having had 7x the error): the E4M3 codes are widened exactly to
+ * bf16 in shared memory between the TMA load and the tensor-core MMAs, and
+ * k_scale / v_scale (as in the write: [1] or [num_kv_heads] by
+ * d->scale_mode, positive) fold into the softmax scale and the output, so
+ * out = softmax(scale * q (k_scale K)^T) (v_scale V) with Q.K^T the exact
+ * products of bf16 q and the codes summed in f32.  No workspace: nothing
+ * beyond the cache is read or written.  bf16 caches take NULL scales.
+ * This build: head_size 192 and head_size_v 128, num_q_heads / num_kv_heads
+ * dividing 128, block_size a power of two >= 8, K at a 64-element column
+ * offset and V at a 16-byte one; otherwise PKV_EUNSUPPORTED.  PKV_EINVAL for null
  * pointers, softmax_scale <= 0 or inconsistent sizes, and when q, cache or
  * out is not device memory of the current device (pinned or mapped host
  * memory, managed memory, another GPU's memory): the kernel's tensor maps
@@ -186,10 +194,12 @@ size_t pkv_prefill_fp8_workspace_bytes(int num_seqs, int max_blocks_per_seq,
                                        const pkv_cache_desc *d);
 
 /*
- * pkv_paged_attn_prefill_fp8 -- the prefill over an FP8 E4M3 cache (the
- * MiMo model card's production setting, "What the kernels do": FP8 K/V,
- * with Q.K^T kept in 16-bit; its FP8 Q.K^T had 7x the error).  Two passes on
- * `stream`:
+ * pkv_paged_attn_prefill_fp8 -- the prefill over an FP8 E4M3 cache in two
+ * passes, for callers that can give it a workspace: the same result as
+ * pkv_paged_attn_prefill on the FP8 cache (which widens the codes inside
+ * the kernel and needs no workspace), faster, because the tensor-core MMAs
+ * then read bf16 slabs that no widening step in shared memory competes
+ * with.  Two passes on `stream`:
  *   1. every page a sequence uses (block_table[b][j], j < ceil(seq_lens[b] /
  *      block_size)) is copied into the workspace as its E4M3 codes widened
  *      to bf16 (exact), with a remapped block table;
@@ -229,7 +239,8 @@ int pkv_paged_attn_prefill_fp8(const void *q, int num_q_heads, int num_tokens,
  * s_j = softmax_scale * q.k_j over the row's visible keys, h the row's query
  * head.  sinks: float32 [num_q_heads], device memory; a sink of -inf is no
  * sink; NULL gives pkv_paged_attn_prefill's result.  Other arguments,
- * layouts, status codes and supported shapes as in pkv_paged_attn_prefill.
+ * layouts, status codes and supported shapes (bf16 and FP8 caches) as in
+ * pkv_paged_attn_prefill.
  */
 int pkv_paged_attn_prefill_sink(const void *q, int num_q_heads, int num_tokens,
                                 const void *cache, const pkv_cache_desc *d,
@@ -472,8 +483,7 @@ int pkv_decode_suggest_splits(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /*
  * pkv_supports -- whether this build serves a K/V head-size pair for a cache
- * dtype in each call: bit 0 write, bit 1 prefill (pkv_paged_attn_prefill for
- * bf16 caches, pkv_paged_attn_prefill_fp8 for FP8 ones), bit 2 decode.
+ * dtype in each call: bit 0 write, bit 1 prefill, bit 2 decode.
  * Mirrors the per-backend capability check of vLLM PR #64064 ("Details":
  * v <= k is what a page split at head_size can serve); 0 when v > k.
  */

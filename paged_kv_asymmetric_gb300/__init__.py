@@ -105,16 +105,16 @@ def _lib():
         lib.pkv_paged_attn_decode_balanced.argtypes = [P, I, I, P, D, P, I, P, P, I, I,
                                                        F, P, P, I, I, P, P, P]
         lib.pkv_decode_balanced_ranges.argtypes = [D]
+        lib.pkv_prefill_fp8_workspace_bytes.argtypes = [I, I, D]
+        lib.pkv_prefill_fp8_workspace_bytes.restype = ctypes.c_size_t
+        lib.pkv_paged_attn_prefill_fp8.argtypes = [P, I, I, P, D, P, I, P, P, I, F, P, P,
+                                                   P, P, ctypes.c_size_t, P, P]
         lib.pkv_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_splitkv_reduce.argtypes = [P, P, I, I, I, P, P, P]
         lib.pkv_splitkv_reduce_sink.argtypes = [P, P, I, I, I, P, I, P, P, P]
         lib.pkv_paged_attn_prefill_sink.argtypes = [P, I, I, P, D, P, I, P, P, I,
                                                     F, P, P, P, P, P]
-        lib.pkv_prefill_fp8_workspace_bytes.argtypes = [I, I, D]
-        lib.pkv_prefill_fp8_workspace_bytes.restype = ctypes.c_size_t
-        lib.pkv_paged_attn_prefill_fp8.argtypes = [P, I, I, P, D, P, I, P, P, I, F, P, P,
-                                                   P, P, ctypes.c_size_t, P, P]
         lib.pkv_decode_suggest_splits.argtypes = [I, I, I, I, I, I]
         lib.pkv_supports.argtypes = [I, I, I]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I), P]
@@ -204,10 +204,11 @@ def paged_attn_prefill(q, cache: Cache, block_table, seq_lens,
                        k_scale=None, v_scale=None, stream=None, sinks=None,
                        workspace=None):
     """q: bf16 [T, Hq, dk]; returns out bf16 [T, Hq, dv].  ``sinks``: float32
-    [Hq] CUDA tensor of attention-sink logits (pkv_paged_attn_prefill_sink),
-    or None.  An FP8 cache goes through pkv_paged_attn_prefill_fp8 with
-    ``workspace`` (a uint8 CUDA tensor of at least
-    prefill_fp8_workspace_bytes(...) bytes; one is allocated when None)."""
+    [Hq] CUDA tensor of attention-sink logits, or None.  An FP8 cache takes
+    k_scale / v_scale (float32 CUDA tensors); with ``workspace`` None its
+    codes are widened in the kernel (pkv_paged_attn_prefill), with a uint8
+    CUDA tensor of at least prefill_fp8_workspace_bytes(...) bytes the
+    two-pass form runs (pkv_paged_attn_prefill_fp8)."""
     _attn_common(q, block_table, seq_lens, query_start_loc)
     T, Hq, _ = q.shape
     if out is None:
@@ -220,11 +221,7 @@ def paged_attn_prefill(q, cache: Cache, block_table, seq_lens,
     if sinks is not None:
         assert sinks.dtype == torch.float32 and sinks.is_contiguous()
         assert tuple(sinks.shape) == (Hq,)
-    if cache.desc.dtype == FP8_E4M3:
-        n = prefill_fp8_workspace_bytes(int(seq_lens.shape[0]), int(block_table.shape[1]),
-                                        cache)
-        if workspace is None:
-            workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    if workspace is not None:
         nb = workspace.numel() * workspace.element_size()
         _check("pkv_paged_attn_prefill_fp8", _lib().pkv_paged_attn_prefill_fp8(
             *args, _ptr(sinks), _ptr(workspace), nb, _ptr(out), _stream(stream)))

@@ -235,9 +235,11 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
   if (128 % G != 0) return PKV_EUNSUPPORTED;
   const int bs = d->block_size;
   if (bs < 8 || (bs & (bs - 1)) != 0) return PKV_EUNSUPPORTED;
-  // TMA tiles: 16-byte aligned base and row strides, 64-element K/V boxes
-  if (!aligned16(cache) || !aligned16(q) || (d->row_elems * 2) % 16 != 0 ||
-      d->k_off % 64 != 0 || d->v_off % 8 != 0)
+  // TMA tiles: 16-byte aligned base and row strides, 64-column K/V boxes
+  // whose first byte sits on a 16-byte boundary
+  const int esz = d->dtype == PKV_FP8_E4M3 ? 1 : 2;
+  if (!aligned16(cache) || !aligned16(q) || (d->row_elems * esz) % 16 != 0 ||
+      d->k_off % 64 != 0 || (d->v_off * esz) % 16 != 0)
     return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
   // q and the cache are read through tensor maps (K/V boxes multicast to
@@ -254,11 +256,13 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
                                   k_scale, v_scale, err);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.sinks = sinks;
-  if (fold_scale_mode >= 0) {  // FP8 codes widened to bf16: the scales fold in
+  // FP8 cache: the E4M3 codes are widened to bf16 in the kernel, k_scale
+  // folds into the softmax scale and v_scale into the output; the same fold
+  // for a bf16 cache that holds widened E4M3 codes (the two-pass form)
+  p.fold_scales = d->dtype == PKV_FP8_E4M3 ? 1 : 0;
+  if (fold_scale_mode >= 0) {
     p.fold_scales = 1;
     p.scale_mode = fold_scale_mode;
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
   }
   cudaError_t e = pkv::launch_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_EUNSUPPORTED;
@@ -731,9 +735,7 @@ int pkv_supports(int head_size, int head_size_v, int dtype) {
   if (head_size < 1 || head_size_v < 1 || head_size_v > head_size) return 0;
   if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return 0;
   int bits = 1;  // the write takes any K / V sizes
-  // prefill: pkv_paged_attn_prefill for bf16 caches, pkv_paged_attn_prefill_fp8
-  // (the same kernel on the widened codes) for FP8 ones
-  if (pkv::prefill_supported(head_size, head_size_v, PKV_BF16)) bits |= 2;
+  if (pkv::prefill_supported(head_size, head_size_v, dtype)) bits |= 2;
   if (pkv::decode_supported(head_size, head_size_v, dtype)) bits |= 4;
   return bits;
 }

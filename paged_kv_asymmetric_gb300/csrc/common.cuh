@@ -122,6 +122,19 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Named barrier over `count` threads (a multiple of 32).
+// OR of `pred` over the `count` threads that meet at named barrier `id`;
+// every participant gets the same answer.
+__device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " barrier.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count));
 }

@@ -224,19 +224,6 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
 
-// OR of `pred` over the `count` threads that meet at named barrier `id`;
-// every participant gets the same answer.
-__device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " barrier.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 // Rows of one TMA box: the largest power of two <= kpc that divides the
 // block size, so that a chunk's boxes tile it and none straddles a page.
 __host__ __device__ constexpr int box_rows_for(int bs, int kpc) {

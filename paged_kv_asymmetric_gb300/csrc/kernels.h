@@ -62,9 +62,9 @@ struct AttnParams {
   // prefill: one attention-sink logit per query head (nullable), an extra
   // term exp(sink) in each row's softmax denominator
   const float* sinks;
-  // prefill: the cache holds FP8 codes widened to bf16 (the FP8 prefill's
-  // workspace); k_scale is folded into the softmax scale and v_scale into
-  // the output, per KV head (or per tensor)
+  // prefill over an FP8 cache, or over a bf16 cache of widened E4M3 codes:
+  // k_scale is folded into the softmax scale and v_scale into the output,
+  // per KV head (or per tensor)
   int fold_scales;
 };
 

@@ -76,11 +76,15 @@ enum {
   B_FINAL = B_OFREE0 + 2,
   B_SLAB_FULL0,
   B_SLAB_EMPTY0 = B_SLAB_FULL0 + NSLAB,
-  NBAR = B_SLAB_EMPTY0 + NSLAB
+  // FP8 cache: a slab's E4M3 codes have been widened to bf16 in place
+  B_SLAB_READY0 = B_SLAB_EMPTY0 + NSLAB,
+  NBAR = B_SLAB_READY0 + NSLAB
 };
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem base, abort word
 constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
 constexpr int THREADS = 384;  // 4 control warps + 2 softmax warpgroups
+// FP8 cache: one more warpgroup (warps 12..15) widens the E4M3 slabs
+constexpr int THREADS_F8 = 512;
 constexpr uint32_t TMEM_COLS = 512;
 // tensor-memory columns: S and O of tile A, then of tile B
 __device__ __forceinline__ uint32_t tm_s(int x) { return x ? 256u : 0u; }
@@ -153,6 +157,64 @@ __device__ __forceinline__ bool get_unit(const AttnParams& p, int TQ, int idx,
   return false;
 }
 
+// FP8 cache: one ring slab's 128 key rows x 64 columns, landed by TMA as E4M3
+// codes in the slab's upper half (row r at byte 8192 + 64 r), widened in
+// place to the bf16 slab the MMAs read (row r at byte 128 r, 16-byte chunk c
+// at chunk c ^ (r & 7): the 128-byte swizzle of the bf16 boxes).  An E4M3
+// value has 4 significant bits and an exponent within bf16's range, so
+// E4M3 -> f16 -> bf16 is exact (NaN stays NaN).  Run by the 64 threads of
+// the widening warpgroup (ct = 0..127, named barrier kWidenBar).  Output row r
+// covers the input of rows 2r - 128 and 2r - 127, so the rows go in three
+// steps: rows 0..63 (their output lies below all input); rows 64..95 (over
+// the input of rows 0..63, already read) while rows 96..127's input is read
+// into registers; then rows 96..127.
+constexpr int kWidenBar = 1;
+constexpr int kWidenThreads = 128;
+
+__device__ __forceinline__ uint4 widen8(uint2 w) {
+  const uint32_t in[2] = {w.x, w.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t f16 = e4m3x2_to_f16x2(static_cast<uint16_t>(in[k] >> (16 * h)));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16));
+      o[2 * k + h] = pack_bf16x2(f.x, f.y);
+    }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ void widen_slab(uint8_t* slab, int ct) {
+  auto src = [&](int row, int c) {
+    return *reinterpret_cast<const uint2*>(slab + 8192 + 64 * row + 8 * c);
+  };
+  auto dst = [&](int row, int c) {
+    return reinterpret_cast<uint4*>(slab + 128 * row + 16 * (c ^ (row & 7)));
+  };
+  constexpr int kRows64 = 512 / kWidenThreads;  // 16-byte outputs per thread, rows 0..63
+  constexpr int kRows32 = 256 / kWidenThreads;  // and per 32 rows
+#pragma unroll
+  for (int i = 0; i < kRows64; ++i) {  // rows 0..63
+    const int q = ct + kWidenThreads * i;
+    *dst(q >> 3, q & 7) = widen8(src(q >> 3, q & 7));
+  }
+  named_barrier(kWidenBar, kWidenThreads);
+  uint2 hold[kRows32];
+#pragma unroll
+  for (int i = 0; i < kRows32; ++i) {  // rows 64..95; rows 96..127 read
+    const int q = ct + kWidenThreads * i;
+    *dst(64 + (q >> 3), q & 7) = widen8(src(64 + (q >> 3), q & 7));
+    hold[i] = src(96 + (q >> 3), q & 7);
+  }
+  named_barrier(kWidenBar, kWidenThreads);
+#pragma unroll
+  for (int i = 0; i < kRows32; ++i) {  // rows 96..127
+    const int q = ct + kWidenThreads * i;
+    *dst(96 + (q >> 3), q & 7) = widen8(hold[i]);
+  }
+}
+
 // The k-th unit of this cluster.  Units are numbered longest-first and dealt
 // in rounds over the clusters, alternately forwards and backwards, so that
 // every cluster's total work is about the same.
@@ -162,7 +224,11 @@ __device__ __forceinline__ int unit_index(int k) {
   return k * ncl + ((k & 1) ? ncl - 1 - cid : cid);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// F8: the cache holds E4M3 codes; they are widened to bf16 in shared memory
+// by warps 2 and 3 between the TMA fill and the MMAs (k_scale and v_scale
+// fold into the softmax scale and the output, p.fold_scales).
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap kv_map,
                    const AttnParams p) {
@@ -214,7 +280,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   // enough to hold a whole S row per thread.
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
+  if constexpr (F8)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
+  else
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ------
     // Fill order per item: K_0, V_0, K_1, V_1, ...  Lane i owns box i of a
@@ -238,8 +307,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int lim = it.L - kt * BN;  // keys of the tile inside the sequence
       const int nb = min(nbox, (lim + box_rows - 1) / box_rows);
       const uint32_t full = bar(B_SLAB_FULL0 + slot);
+      constexpr int kRowBytes = F8 ? 64 : 128;  // one box row: 64 columns
       if (lane == 0)
-        tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * 128));
+        tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * kRowBytes));
       __syncwarp();
       // each box is copied by one rank into both CTAs (ranks alternate)
       if (lane < nb && ((lane + static_cast<int>(f)) % CLUSTER) == rank) {
@@ -250,7 +320,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           set_dev_error(p.err, PKV_EDEV_RANGE);
           page = p.num_blocks;  // out-of-range box: TMA fills zeros
         }
-        const uint32_t dst = sbase + RING_OFF + slot * SLAB + lane * box_rows * 128;
+        const uint32_t dst = sbase + RING_OFF + slot * SLAB + (F8 ? 8192 : 0) +
+                             lane * box_rows * kRowBytes;
         if (p.layout == PKV_NHD)
           tc5::tma_load_4d_mc(dst, &kv_map, col, it.g, off, page, full, CLUSTER_MASK);
         else
@@ -315,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc5::mma_commit_mc(bar(B_SLAB_EMPTY0 + slot), CLUSTER_MASK);
     };
     auto wait_fill = [&](uint32_t fill) {
-      return wait(B_SLAB_FULL0 + fill % NSLAB, (fill / NSLAB) & 1u);
+      return wait((F8 ? B_SLAB_READY0 : B_SLAB_FULL0) + fill % NSLAB, (fill / NSLAB) & 1u);
     };
     // S_x = Q_x K_j^T
     auto issue_s = [&](int x, uint32_t fb, int j) {
@@ -390,6 +461,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc5::mma_commit(bar(B_FINAL));
     tc5::mbar_wait(bar(B_FINAL), 0, abort_flag, p.err, /*honor_abort=*/false);
   }
+  } else if (F8 && warp >= 12) {
+    // Registers: the FP8 block is launched with 512 x 128; the control
+    // warpgroup keeps 104, the widening warpgroup 40, and the two softmax
+    // warpgroups take 184 (128 x 104 + 128 x 40 + 256 x 184 = 65,536).
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+    // ------------------------------------------------ E4M3 widening -----
+    // Warps 12..15 take the ring fills in the producer's order: wait for a
+    // fill to land, widen it in place, make the bf16 rows visible to the
+    // tensor core, and mark the slab ready.
+    const int ct = threadIdx.x - 384;
+    uint32_t f = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Item it;
+      if (!get_unit(p, TQ, unit_index(k), rank, it)) break;
+      const uint32_t nf = FILLS_PER_TILE * static_cast<uint32_t>(it.ntiles);
+      for (uint32_t i = 0; i < nf; ++i, ++f) {
+        const uint32_t slot = f % NSLAB;
+        const bool w = tc5::mbar_wait(bar(B_SLAB_FULL0 + slot), (f / NSLAB) & 1u, abort_flag,
+                                      p.err);
+        // all four warps take the same decision to stop
+        if (barrier_or(kWidenBar, kWidenThreads, !w)) {
+          ok = false;
+          break;
+        }
+        widen_slab(smem + RING_OFF + slot * SLAB, ct);
+        tc5::fence_proxy_async_smem();
+        named_barrier(kWidenBar, kWidenThreads);
+        if (ct == 0) tc5::mbar_arrive(bar(B_SLAB_READY0 + slot));
+      }
+    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
     // ------------------------------------------------ softmax -----------
@@ -511,7 +613,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           // last tile: zero the V rows of keys past the sequence end
           for (int h = 0; h < VSLABS && ok; ++h) {
             const uint32_t fi = v_fill(fbase, j, h);
-            ok = wwait(bar(B_SLAB_FULL0 + fi % NSLAB), (fi / NSLAB) & 1u);
+            ok = wwait(bar((F8 ? B_SLAB_READY0 : B_SLAB_FULL0) + fi % NSLAB),
+                       (fi / NSLAB) & 1u);
             if (ok && kbase + r >= it.L) {
               uint4* vrow =
                   reinterpret_cast<uint4*>(smem + RING_OFF + (fi % NSLAB) * SLAB + r * 128);
@@ -575,7 +678,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 bool prefill_supported(int head_size, int head_size_v, int dtype) {
-  return head_size == DK && head_size_v == DV && dtype == PKV_BF16;
+  return head_size == DK && head_size_v == DV && (dtype == PKV_BF16 || dtype == PKV_FP8_E4M3);
 }
 
 cudaError_t launch_prefill(const AttnParams& p, int num_sms,
@@ -604,11 +707,16 @@ cudaError_t launch_prefill(const AttnParams& p, int num_sms,
       return cudaErrorInvalidValue;
   }
   const int box_rows = p.block_size < BN ? p.block_size : BN;
+  // bf16: 64-column boxes in the MMAs' 128-byte swizzle; FP8: 64-column
+  // boxes of E4M3 codes landing densely, widened in shared memory
+  const bool f8 = p.dtype == PKV_FP8_E4M3;
   if (!make_cache_tmap(&kv_map, p.cache, p.dtype, p.layout, p.num_blocks,
-                       p.block_size, p.num_kv_heads, p.row_elems, 64, box_rows))
+                       p.block_size, p.num_kv_heads, p.row_elems, 64, box_rows,
+                       /*swizzle64=*/false, /*no_swizzle=*/f8))
     return cudaErrorInvalidValue;
-  static int attr_set[64] = {0};
-  cudaError_t e = ensure_smem_attr(prefill_kernel, SMEM_BYTES, attr_set);
+  auto kernel = f8 ? prefill_kernel<true> : prefill_kernel<false>;
+  static int attr_set[2][64] = {{0}};
+  cudaError_t e = ensure_smem_attr(kernel, SMEM_BYTES, attr_set[f8 ? 1 : 0]);
   if (e != cudaSuccess) return e;
   // Persistent: as many CTA pairs (clusters) as can be resident at once.
   cudaLaunchAttribute attr[1];
@@ -618,7 +726,7 @@ cudaError_t launch_prefill(const AttnParams& p, int num_sms,
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CLUSTER * CLUSTER));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(f8 ? THREADS_F8 : THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -629,14 +737,14 @@ cudaError_t launch_prefill(const AttnParams& p, int num_sms,
   static int max_clusters[64] = {0};
   int ncl = dev < 64 ? max_clusters[dev] : 0;
   if (ncl == 0) {
-    e = cudaOccupancyMaxActiveClusters(&ncl, prefill_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&ncl, kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (ncl < 1) return cudaErrorNotSupported;
     if (dev < 64) max_clusters[dev] = ncl;
   }
   if (ncl > num_sms / CLUSTER) ncl = num_sms / CLUSTER;
   cfg.gridDim = dim3(static_cast<unsigned>(ncl * CLUSTER));
-  e = cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, kv_map, p);
+  e = cudaLaunchKernelEx(&cfg, kernel, q_map, kv_map, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

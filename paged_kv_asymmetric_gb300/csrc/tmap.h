@@ -28,14 +28,16 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
 }
 
 // A 4-D map over the cache whose boxes are `box_cols` row elements wide (at
-// most one swizzle span: 128 bytes, or 64 with swizzle64) and `box_rows`
-// token slots high, for one KV head of one page.  Coordinates: NHD (col,
+// most one swizzle span: 128 bytes, or 64 with swizzle64; rows land densely
+// with no_swizzle) and `box_rows` token slots high, for one KV head of one
+// page.  Coordinates: NHD (col,
 // head, slot, page), HND (col, slot, head, page).  Columns past row_elems
 // read as zero.
 inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
                             int layout, int num_blocks, int block_size,
                             int num_kv_heads, int row_elems, int box_cols,
-                            int box_rows, bool swizzle64 = false) {
+                            int box_rows, bool swizzle64 = false,
+                            bool no_swizzle = false) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encode_fn();
   if (encode == nullptr) return false;
   const cuuint64_t e = dtype == PKV_FP8_E4M3 ? 1 : 2;
@@ -59,7 +61,8 @@ inline bool make_cache_tmap(CUtensorMap* map, const void* cache, int dtype,
                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                 4, const_cast<void*>(cache), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE,
-                swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                no_swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                           : swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

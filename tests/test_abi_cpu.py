@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_supports_mirrors_v_le_k(lib):
     assert pkv.supports(192, 128) == 7
-    assert pkv.supports(192, 128, pkv.FP8_E4M3) == 7   # fp8 prefill: pkv_paged_attn_prefill_fp8
+    assert pkv.supports(192, 128, pkv.FP8_E4M3) == 7   # FP8 prefill widens in the kernel
     assert pkv.supports(576, 512) == 5
     assert pkv.supports(128, 192) == 0                  # V wider than K
     assert pkv.supports(64, 64) == 1                    # write only
@@ -220,6 +220,24 @@ def test_reduce_sink_rejects_bad_arguments(lib):
     assert f(DUMMY, DUMMY, 2, 0, 128, DUMMY, 4, None, None, None) == pkv.OK
 
 
+def test_prefill_fp8_rejects_bad_arguments(lib):
+    d8 = _desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)
+
+    def call(d, ks=DUMMY, vs=DUMMY, **kw):
+        a = dict(q=DUMMY, Hq=16, T=4, scale=0.1, out=DUMMY)
+        a.update(kw)
+        return lib.pkv_paged_attn_prefill(
+            a["q"], a["Hq"], a["T"], DUMMY, ctypes.byref(d), DUMMY, 4, DUMMY,
+            DUMMY, 1, ctypes.c_float(a["scale"]), ks, vs, a["out"], None)
+    assert call(d8, ks=None) == pkv.EINVAL                   # scales missing
+    assert call(d8, vs=None) == pkv.EINVAL
+    assert call(d8, scale=-1.0) == pkv.EINVAL
+    assert call(d8, out=None) == pkv.EINVAL
+    assert call(_desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD,
+                      v_off=200, row_elems=328)) == pkv.EUNSUPPORTED  # V not on 16 bytes
+    assert call(d8, T=0) == pkv.OK                           # nothing to do
+
+
 def test_prefill_fp8_workspace_size(lib):
     d8 = _desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)   # block 16, 4 heads, row 320
     f = lib.pkv_prefill_fp8_workspace_bytes
@@ -233,7 +251,7 @@ def test_prefill_fp8_workspace_size(lib):
     assert f(3, 5, None) == 0
 
 
-def test_prefill_fp8_rejects_bad_arguments(lib):
+def test_prefill_fp8_two_pass_rejects_bad_arguments(lib):
     d8 = _desc(dtype=pkv.FP8_E4M3, scale_mode=pkv.SCALE_HEAD)
     f = lib.pkv_prefill_fp8_workspace_bytes
     f.restype = ctypes.c_size_t

@@ -1,9 +1,10 @@
-"""The prefill over an FP8 E4M3 cache (pkv_paged_attn_prefill_fp8: the
-batch's pages widened to bf16 codes in a workspace, then the tcgen05
-prefill with the scales folded in) against the oracle, which reads the
-same cache through its own E4M3 decoder.  FP8-KV tolerance: atol 3e-2.
-Unwritten cache bytes hold NaN codes, so the partly filled last page of a
-sequence exercises the tail masking through the widened copy."""
+"""The prefill over an FP8 E4M3 cache against the oracle, which reads the
+same cache through its own E4M3 decoder, in both forms: pkv_paged_attn_prefill
+(the E4M3 codes widened to bf16 in shared memory between the TMA load and
+the tcgen05 MMAs, no workspace) and pkv_paged_attn_prefill_fp8 (the pages
+widened into a workspace first); the scales fold in.  FP8-KV tolerance:
+atol 3e-2.  Unwritten cache bytes hold NaN codes, so the partly filled last
+page of a sequence exercises the tail masking."""
 from __future__ import annotations
 
 import numpy as np
@@ -36,14 +37,19 @@ CASES = {
 }
 
 
-def _run(w, tokens=None, seqs=None, sinks=None):
+def _run(w, tokens=None, seqs=None, sinks=None, two_pass=False):
     dw = wl.to_device(w)
     gpu_path.write_all(dw)
     gpu_path.device_error()
     st = None if sinks is None else torch.from_numpy(sinks).cuda()
+    ws = None
+    if two_pass:
+        n = pkv.prefill_fp8_workspace_bytes(w.num_seqs, dw.block_table.shape[1], dw.cache)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
     out = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
                                  dw.query_start_loc, w.softmax_scale,
-                                 k_scale=dw.k_scale, v_scale=dw.v_scale, sinks=st)
+                                 k_scale=dw.k_scale, v_scale=dw.v_scale, sinks=st,
+                                 workspace=ws)
     torch.cuda.synchronize()
     assert gpu_path.device_error() == pkv.EDEV_NONE
     o, _ = gpu_path.oracle_rows(w, tokens=tokens, seqs=seqs, sinks=sinks)
@@ -54,25 +60,27 @@ def _run(w, tokens=None, seqs=None, sinks=None):
     return dw, out
 
 
+@pytest.mark.parametrize("two_pass", [False, True])
 @pytest.mark.parametrize("name", list(CASES))
-def test_fp8_prefill_small(name):
-    _run(CASES[name]())
+def test_fp8_prefill_small(name, two_pass):
+    _run(CASES[name](), two_pass=two_pass)
 
 
-def test_fp8_prefill_with_sinks():
+def test_fp8_prefill_two_forms_agree():
+    """Both forms run the same tensor-core prefill on the same bf16 values
+    (exact widening), so their outputs are identical bits."""
     w = CASES["chunked-with-context-b64"]()
     sinks = np.linspace(-3, 3, w.num_q_heads).astype(np.float32)
-    _run(w, sinks=sinks)
-
-
-def test_fp8_prefill_repeatable_and_workspace_checks():
-    w = CASES["ragged-varlen"]()
-    dw, a = _run(w)
-    b = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
-                               dw.query_start_loc, w.softmax_scale,
-                               k_scale=dw.k_scale, v_scale=dw.v_scale)
+    _, a = _run(w, sinks=sinks)
+    _, b = _run(w, sinks=sinks, two_pass=True)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_fp8_prefill_two_pass_workspace_checks():
+    w = CASES["ragged-varlen"]()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
     n = pkv.prefill_fp8_workspace_bytes(w.num_seqs, dw.block_table.shape[1], dw.cache)
     assert n > 0
     small = torch.empty(n - 256, dtype=torch.uint8, device="cuda")
@@ -89,6 +97,48 @@ def test_fp8_prefill_repeatable_and_workspace_checks():
     assert e.value.status == pkv.EINVAL
 
 
+def test_fp8_prefill_with_sinks():
+    w = CASES["chunked-with-context-b64"]()
+    sinks = np.linspace(-3, 3, w.num_q_heads).astype(np.float32)
+    _run(w, sinks=sinks)
+
+
+def test_fp8_prefill_repeatable():
+    w = CASES["ragged-varlen"]()
+    dw, a = _run(w)
+    b = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                               dw.query_start_loc, w.softmax_scale,
+                               k_scale=dw.k_scale, v_scale=dw.v_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_fp8_prefill_matches_bf16_prefill_of_the_widened_codes():
+    """The in-kernel widening is exact: the FP8 prefill equals, bit for bit,
+    the bf16 prefill over a bf16 cache holding the same codes widened on the
+    host (torch's float8_e4m3fn -> bfloat16), with the scales applied to
+    q and the output the way the kernel folds them (here: unit scales)."""
+    w = CASES["chunked-with-context-b64"]()
+    w.k_scale = np.ones_like(w.k_scale)
+    w.v_scale = np.ones_like(w.v_scale)
+    dw, a = _run(w)
+    codes = dw.cache.data.view(torch.float8_e4m3fn)
+    wide = codes.to(torch.bfloat16)
+    desc = pkv.make_desc(dtype=pkv.BF16, layout=dw.cache.desc.layout,
+                         num_blocks=dw.cache.desc.num_blocks,
+                         block_size=dw.cache.desc.block_size,
+                         num_kv_heads=dw.cache.desc.num_kv_heads,
+                         row_elems=dw.cache.desc.row_elems, k_off=dw.cache.desc.k_off,
+                         head_size=dw.cache.desc.head_size, v_off=dw.cache.desc.v_off,
+                         head_size_v=dw.cache.desc.head_size_v)
+    b = pkv.paged_attn_prefill(dw.q, pkv.Cache(wide, desc), dw.block_table, dw.seq_lens,
+                               dw.query_start_loc, w.softmax_scale)
+    torch.cuda.synchronize()
+    fin = torch.isfinite(b.float()).all(dim=-1).all(dim=-1)
+    assert fin.all()
+    assert torch.equal(a, b)
+
+
 def test_fp8_prefill_32k_sampled():
     """32,768 tokens, FP8 cache with per-head scales, in the bench's launch
     shape: the tokens of the bf16 32K test's choice (first and last dealt
@@ -101,3 +151,4 @@ def test_fp8_prefill_32k_sampled():
     toks = prefill_sample_tokens(32768, units, 24, seed=1)
     assert len(toks) * 16 >= 2048
     _run(w, tokens=toks, seqs=[0])
+    _run(w, tokens=toks, seqs=[0], two_pass=True)
