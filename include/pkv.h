@@ -385,6 +385,28 @@ int pkv_paged_attn_decode_fused(const void *q, int num_q_heads, int num_tokens,
                                 pkv_stream_t stream);
 
 /*
+ * pkv_paged_attn_decode_balanced_fused -- pkv_paged_attn_decode_balanced and
+ * the split merge in one launch: every unit writes its segment's partials
+ * and counts itself done in the workspace; the last unit of each (sequence,
+ * KV-head block, 16-row group) to finish merges that sequence's segments (as
+ * many as its ranges) as pkv_splitkv_reduce does into out (bf16
+ * [num_tokens][num_q_heads][head_size_v]) and lse_out (float32
+ * [num_tokens][num_q_heads], or NULL), and resets its counter; the rows of a
+ * sequence with no key are written as 0 (lse -inf).  Segmentation, max_splits
+ * and num_ranges as in pkv_paged_attn_decode_balanced; workspace rules,
+ * partial_o / partial_lse (scratch here) and the fallback past 32 splits (a
+ * second launch) as in pkv_paged_attn_decode_fused.  Status codes as in
+ * those two calls; PKV_EINVAL also for num_ranges < 0.
+ */
+int pkv_paged_attn_decode_balanced_fused(
+    const void *q, int num_q_heads, int num_tokens, const void *cache,
+    const pkv_cache_desc *d, const int32_t *block_table, int max_blocks_per_seq,
+    const int32_t *seq_lens, const int32_t *query_start_loc, int num_seqs,
+    int max_query_len, float softmax_scale, const float *k_scale, const float *v_scale,
+    int max_splits, int num_ranges, float *partial_o, float *partial_lse, void *workspace,
+    size_t workspace_bytes, void *out, float *lse_out, pkv_stream_t stream);
+
+/*
  * pkv_paged_attn_decode_fused_noalloc -- pkv_paged_attn_decode_fused
  * without a caller workspace.  The pages have no counterpart.  It serves
  * callers that cannot allocate device memory for the counters: a serving

@@ -39,6 +39,7 @@ EXPORTED = (
     "pkv_paged_attn_prefill_sink", "pkv_prefill_fp8_workspace_bytes",
     "pkv_paged_attn_prefill_fp8", "pkv_decode_suggest_splits",
     "pkv_paged_attn_decode_balanced", "pkv_decode_balanced_ranges",
+    "pkv_paged_attn_decode_balanced_fused",
     "pkv_supports",
     "pkv_get_device_error", "pkv_selftest_bounded_wait", "pkv_last_cuda_error",
     "pkv_status_string",
@@ -105,6 +106,8 @@ def _lib():
         lib.pkv_paged_attn_decode_balanced.argtypes = [P, I, I, P, D, P, I, P, P, I, I,
                                                        F, P, P, I, I, P, P, P]
         lib.pkv_decode_balanced_ranges.argtypes = [D]
+        lib.pkv_paged_attn_decode_balanced_fused.argtypes = [
+            P, I, I, P, D, P, I, P, P, I, I, F, P, P, I, I, P, P, P, ctypes.c_size_t, P, P, P]
         lib.pkv_prefill_fp8_workspace_bytes.argtypes = [I, I, D]
         lib.pkv_prefill_fp8_workspace_bytes.restype = ctypes.c_size_t
         lib.pkv_paged_attn_prefill_fp8.argtypes = [P, I, I, P, D, P, I, P, P, I, F, P, P,
@@ -282,6 +285,38 @@ def paged_attn_decode_balanced(q, cache: Cache, block_table, seq_lens,
         float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(max_splits),
         int(num_ranges), _ptr(partial_o), _ptr(partial_lse), _stream(stream)))
     return partial_o, partial_lse
+
+
+def paged_attn_decode_balanced_fused(q, cache: Cache, block_table, seq_lens,
+                                     query_start_loc, softmax_scale, max_query_len,
+                                     max_splits, workspace, num_ranges=0, out=None,
+                                     lse_out=None, partial_o=None, partial_lse=None,
+                                     k_scale=None, v_scale=None, stream=None):
+    """Balanced-range decode and split merge in one launch
+    (pkv_paged_attn_decode_balanced_fused).  `workspace`: a zero-filled int32
+    CUDA tensor of at least decode_workspace_bytes(...) bytes, left zero by
+    every call.  Returns (out [T, Hq, dv] bf16, lse_out or None)."""
+    _attn_common(q, block_table, seq_lens, query_start_loc)
+    T, Hq, _ = q.shape
+    dv = cache.desc.head_size_v
+    if partial_o is None:
+        partial_o = torch.empty(max_splits, T, Hq, dv, dtype=torch.float32,
+                                device=q.device)
+    if partial_lse is None:
+        partial_lse = torch.empty(max_splits, T, Hq, dtype=torch.float32,
+                                  device=q.device)
+    if out is None:
+        out = torch.empty(T, Hq, dv, dtype=torch.bfloat16, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pkv_paged_attn_decode_balanced_fused",
+           _lib().pkv_paged_attn_decode_balanced_fused(
+               _ptr(q), Hq, T, _ptr(cache.data), ctypes.byref(cache.desc),
+               _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+               _ptr(query_start_loc), int(seq_lens.shape[0]), int(max_query_len),
+               float(softmax_scale), _ptr(k_scale), _ptr(v_scale), int(max_splits),
+               int(num_ranges), _ptr(partial_o), _ptr(partial_lse), _ptr(workspace),
+               ws_bytes, _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
 
 
 def decode_balanced_ranges(cache: Cache) -> int:

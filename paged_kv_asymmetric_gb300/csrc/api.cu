@@ -517,6 +517,14 @@ int pkv_decode_balanced_ranges(const pkv_cache_desc* d) {
   return default_ranges(p, sms);
 }
 
+int pkv_paged_attn_decode_balanced_fused(
+    const void* q, int num_q_heads, int num_tokens, const void* cache,
+    const pkv_cache_desc* d, const int32_t* block_table, int max_blocks_per_seq,
+    const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+    int max_query_len, float softmax_scale, const float* k_scale, const float* v_scale,
+    int max_splits, int num_ranges, float* partial_o, float* partial_lse, void* workspace,
+    size_t workspace_bytes, void* out, float* lse_out, pkv_stream_t stream);
+
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                   int max_query_len) {
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_query_len < 1 ||
@@ -530,7 +538,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
 namespace {
 
 // The fused decode; with `clear`, the counters it uses are zeroed on the
-// stream first (after every argument has been checked).
+// stream first (after every argument has been checked).  num_ranges >= 0:
+// balanced ranges (0: the default count), else equal segments.
 int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void* cache,
                       const pkv_cache_desc* d, const int32_t* block_table,
                       int max_blocks_per_seq, const int32_t* seq_lens,
@@ -538,7 +547,13 @@ int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void
                       float softmax_scale, const float* k_scale, const float* v_scale,
                       int num_splits, float* partial_o, float* partial_lse, void* workspace,
                       size_t workspace_bytes, void* out, float* lse_out, pkv_stream_t stream,
-                      bool clear) {
+                      bool clear, int num_ranges = -1) {
+  const bool balanced = num_ranges >= 0;
+  if (balanced) {
+    if (num_ranges > (1 << 24)) return PKV_EINVAL;
+    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX) return PKV_EINVAL;
+    if (num_seqs > pkv::kBalancedMaxSeqs) return PKV_EUNSUPPORTED;
+  }
   pkv::AttnParams p{};
   int sms = 0;
   bool launch = false;
@@ -560,6 +575,11 @@ int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void
                          (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0))
     return PKV_EINVAL;
   if (!launch) return PKV_OK;
+  if (balanced) {
+    p.split_ranges = num_ranges > 0 ? num_ranges : default_ranges(p, sms);
+    if (static_cast<int64_t>(p.split_ranges) * pkv::decode_head_blocks(p) > (int64_t{1} << 30))
+      return PKV_EINVAL;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (clear && num_splits <= pkv::kFusedMaxSplits) {
     const cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
@@ -642,6 +662,21 @@ int pkv_paged_attn_decode_fused_noalloc(const void* q, int num_q_heads, int num_
                            partial_o, partial_lse, counters,
                            in_kernel_merge || need <= array_bytes ? array_bytes : need, out,
                            lse_out, stream, /*clear=*/true);
+}
+
+int pkv_paged_attn_decode_balanced_fused(
+    const void* q, int num_q_heads, int num_tokens, const void* cache,
+    const pkv_cache_desc* d, const int32_t* block_table, int max_blocks_per_seq,
+    const int32_t* seq_lens, const int32_t* query_start_loc, int num_seqs,
+    int max_query_len, float softmax_scale, const float* k_scale, const float* v_scale,
+    int max_splits, int num_ranges, float* partial_o, float* partial_lse, void* workspace,
+    size_t workspace_bytes, void* out, float* lse_out, pkv_stream_t stream) {
+  if (num_ranges < 0) return PKV_EINVAL;
+  return decode_fused_impl(q, num_q_heads, num_tokens, cache, d, block_table,
+                           max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                           max_query_len, softmax_scale, k_scale, v_scale, max_splits,
+                           partial_o, partial_lse, workspace, workspace_bytes, out, lse_out,
+                           stream, /*clear=*/false, num_ranges);
 }
 
 int pkv_splitkv_reduce(const float* partial_o, const float* partial_lse,

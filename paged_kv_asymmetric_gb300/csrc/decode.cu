@@ -236,7 +236,9 @@ __host__ __device__ constexpr int box_rows_for(int bs, int kpc) {
 // by its page ids.
 struct Unit {
   int b, hb, s, row0, nrows, qs, qlen, L;
-  int klo, khi, kmax, nch, page_lo, npages, pad0, pad1;
+  // nseg: the segments of the unit's sequence that units write (balanced
+  // ranges; the fused merge counts to it), 0 for equal segments
+  int klo, khi, kmax, nch, page_lo, npages, nseg, pad1;
 };
 static_assert(sizeof(Unit) == 64, "descriptor size");
 
@@ -277,7 +279,7 @@ __device__ __forceinline__ void unit_params_pages(const AttnParams& p, int b, in
   un.nch = un.kmax > un.klo ? (un.kmax - un.klo + KPC - 1) / KPC : 0;
   un.page_lo = page_lo;
   un.npages = page_hi - page_lo;
-  un.pad0 = un.pad1 = 0;
+  un.nseg = un.pad1 = 0;
 }
 
 // Unit u's parameters under equal segments, for sequence b (the rank-u /
@@ -313,11 +315,14 @@ __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un
   float* wb = reinterpret_cast<float*>(smem + C::WBUF_OFF);
   volatile int* flag =
       reinterpret_cast<volatile int*>(smem + C::WBUF_OFF + C::HPC * 16 * kFusedMaxSplits * 4);
+  // units that write the rows: every split (equal segments), or the
+  // sequence's ranges (balanced)
+  const int S = un.nseg > 0 ? un.nseg : p.num_splits;
   named_barrier(1, NT);  // the unit's partials are written
   if (ctid == 0) {
     __threadfence();
     const int key = (un.b * HB + un.hb) * RG + un.row0 / 16;
-    const int last = atomicAdd(p.counters + key, 1) == p.num_splits - 1;
+    const int last = atomicAdd(p.counters + key, 1) == S - 1;
     if (last) {
       p.counters[key] = 0;  // zero again for the next call
       __threadfence();
@@ -326,7 +331,6 @@ __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un
   }
   named_barrier(1, NT);
   if (!*flag) return;
-  const int S = p.num_splits;
   const int64_t TH = static_cast<int64_t>(p.num_tokens) * p.num_q_heads;
   const int G = p.group;
   const int nr = C::HPC * un.nrows;
@@ -566,6 +570,18 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
           const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
           p.partial_lse[(static_cast<int64_t>(sg) * T + q0) * p.num_q_heads + rr] = -INFINITY;
         }
+        // fused merge: a sequence without keys has no unit to merge its
+        // rows, so they are written here (0, lse -inf)
+        if (p.fused && nseg == 0) {
+          for (int i = lane; i < rows * (C::DV / 2); i += 32) {
+            const int rr = i / (C::DV / 2), c2 = i - rr * (C::DV / 2);
+            reinterpret_cast<uint32_t*>(p.out + (static_cast<int64_t>(q0) * p.num_q_heads + rr) *
+                                                    C::DV)[c2] = 0u;
+          }
+          if (p.lse_out != nullptr)
+            for (int i = lane; i < rows; i += 32)
+              p.lse_out[static_cast<int64_t>(q0) * p.num_q_heads + i] = -INFINITY;
+        }
       }
     }
     // work item, sequence, row group of the piece, the piece's pages
@@ -679,6 +695,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
         unit_params_pages<KPC>(p, b, bi % us.HB, bj,
                                static_cast<int>(bi / us.HB - gst[b] / bR), bq0, bq1, bL, bplo,
                                bphi, un);
+        un.nseg = static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1);
         if (++bj == us.RG) bpiece = next_piece();
         if (un.s >= p.num_splits) {  // excluded by R >= Rmin; never written past the partials
           set_dev_error(p.err, PKV_EDEV_RANGE);

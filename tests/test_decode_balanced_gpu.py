@@ -128,3 +128,66 @@ def test_balanced_verify_fp8_full():
     _, pl, out, lse = _decode(dw, 16, 0)
     _check_out(w, out, lse)
     assert np.isneginf(gpu_path.host(pl)[:, 64:]).all()
+
+
+# ------------------------------------------- balanced ranges, fused merge ----
+
+def _fused(dw, S, W, ws):
+    w = dw.w
+    T, Hq = w.num_tokens, w.num_q_heads
+    lse = torch.empty(T, Hq, dtype=torch.float32, device=dw.q.device)
+    out, _ = pkv.paged_attn_decode_balanced_fused(
+        dw.q, dw.cache, dw.block_table, dw.seq_lens, dw.query_start_loc, w.softmax_scale,
+        max(1, w.max_query_len), S, ws, num_ranges=W, lse_out=lse,
+        k_scale=dw.k_scale, v_scale=dw.v_scale)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _workspace(w):
+    n = pkv.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                   max(1, w.max_query_len))
+    return torch.zeros(max(1, n // 4), dtype=torch.int32, device="cuda")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("S,W", [(4, 3), (16, 0), (8, 1000), (40, 0)])
+def test_balanced_fused_small(name, S, W):
+    """The merge inside the launch gives the whole rows (the oracle), twice in
+    a row with the same workspace (every counter is left at zero); past 32
+    segments the merge runs as a second launch."""
+    w = SMALL[name]()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    ws = _workspace(w)
+    out, lse = _fused(dw, S, W, ws)
+    assert int(ws.abs().sum()) == 0
+    out2, lse2 = _fused(dw, S, W, ws)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    _check_out(w, out, lse)
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_fused_mixed_lengths_and_empty_sequences():
+    w = wl.make_workload("mixf", seq_lens=[5000, 3, 0, 40, 0, 700, 17],
+                         q_lens=[1, 1, 4, 2, 1, 4, 1], block_size=16, seed=23)
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    ws = _workspace(w)
+    for S, W in ((16, 0), (32, 5), (3, 152)):
+        out, lse = _fused(dw, S, W, ws)
+        _check_out(w, out, lse)
+        empty = gpu_path.tokens_of(w, [2, 4])
+        assert (gpu_path.host(out)[empty] == 0).all()
+        assert np.isneginf(gpu_path.host(lse)[empty]).all()
+    assert int(ws.abs().sum()) == 0
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_fused_batched_decode_full():
+    """The headline batched decode in one launch: every row against the oracle."""
+    w = wl.batched_decode()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    out, lse = _fused(dw, w.max_splits, 0, _workspace(w))
+    _check_out(w, out, lse)
