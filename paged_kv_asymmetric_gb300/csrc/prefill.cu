@@ -562,13 +562,16 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
         }
         float mx;
         {
+          // eight chains of three-input maxima
           float mc[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) mc[k] = sv[k];
 #pragma unroll
-          for (int c = 8; c < BN; ++c) mc[c & 7] = fmaxf(mc[c & 7], sv[c]);
-          mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
-                     fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+          for (int c = 8; c < BN; c += 16)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], sv[c + k], sv[c + 8 + k]);
+          mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                     fmaxf(mc[6], mc[7]));
         }
         const float m_new = fmaxf(m, mx * scale_log2);
         // The rescale touches O with warp-collective tensor-memory loads and
@@ -592,21 +595,32 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           m = m_new;
         }
         const float base = m == -INFINITY ? 0.f : m;
-        // P (bf16) over the first 64 columns of S
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // P (bf16) over the first 64 columns of S; the exponent arguments
+        // and the running sums go two at a time (packed f32x2)
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t nb2 = f2_pack(-base, -base);
+        uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_exp2(fmaf(sv[32 * c + 2 * k], scale_log2, -base));
-            const float p1 = fast_exp2(fmaf(sv[32 * c + 2 * k + 1], scale_log2, -base));
-            ls[k & 3] += p0 + p1;
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(sv[32 * c + 2 * k], sv[32 * c + 2 * k + 1]), sc2, nb2),
+                      a0, a1);
+            const float p0 = fast_exp2(a0);
+            const float p1 = fast_exp2(a1);
+            ls2[k & 1] = f2_add(ls2[k & 1], f2_pack(p0, p1));
             pk[k] = pack_bf16x2(p0, p1);
           }
           tc5::tmem_st_32x32b_x16(ts + 16 * c, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(ls2[0], s0, s1);
+          f2_unpack(ls2[1], s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
         tc5::tmem_wait_st();
         bool zeroed = false;
         if (x == 0 && kbase + BN > it.L) {
