@@ -274,10 +274,11 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
   const int box_rows = bs < BN ? bs : BN;
   const int nbox = BN / box_rows;
 
-  // Registers: the block is launched with 384 x 168; the control warpgroup
-  // (producer, MMA issuer, two idle warps) keeps 120 per thread and the two
-  // softmax warpgroups take 184 (128 x 120 + 256 x 184 = 62,464 <= 64,512),
-  // enough to hold a whole S row per thread.
+  // Registers: the bf16 block is launched with 384 x 168; the control
+  // warpgroup (producer, MMA issuer, two idle warps) keeps 120 per thread and
+  // the two softmax warpgroups take 192 (128 x 120 + 256 x 192 = 64,512),
+  // enough to hold a whole S row per thread.  The FP8 block's split is given
+  // with its widening warpgroup below.
 
   if (warp < 4) {
   if constexpr (F8)
@@ -493,7 +494,12 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
+    // bf16 block: 384 x 168 at launch, control 120, softmax 192
+    // (128 x 120 + 256 x 192 = 64,512); FP8 block: softmax 184 (above)
+    if constexpr (F8)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
+    else
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
     // ------------------------------------------------ softmax -----------
     // Warps 4..7 own query tile A, warps 8..11 tile B; one thread per row.
     const int x = (warp - 4) >> 2;                 // query tile of this warp
