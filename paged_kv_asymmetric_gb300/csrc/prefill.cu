@@ -582,23 +582,19 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
         const float m_new = fmaxf(m, mx * scale_log2);
         // The rescale touches O with warp-collective tensor-memory loads and
         // stores, so it is decided per warp; PV(j-1) has completed (the
-        // commit behind S(j) covers it).
+        // commit behind S(j) covers it).  It runs after the exponentials,
+        // once S is no longer held in registers, and before P is published,
+        // so the next P.V MMA sees the rescaled O.
         const bool need = j > 0 && m_new > m + kRescaleThreshold;
+        bool rescale = false;
+        float alpha = 1.f;
         if (j == 0) {
           m = m_new;
         } else if (__any_sync(0xffffffffu, need)) {
-          const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m - m_new);
-#pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t v[32];
-            tc5::tmem_ld_32x32b_x32(to + 32 * c, v);
-            tc5::tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tc5::tmem_st_32x32b_x32(to + 32 * c, v);
-          }
+          alpha = m_new == -INFINITY ? 1.f : fast_exp2(m - m_new);
           l *= alpha;
           m = m_new;
+          rescale = true;
         }
         const float base = m == -INFINITY ? 0.f : m;
         // P (bf16) over the first 64 columns of S; the exponent arguments
@@ -626,6 +622,17 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           f2_unpack(ls2[0], s0, s1);
           f2_unpack(ls2[1], s2, s3);
           l += (s0 + s1) + (s2 + s3);
+        }
+        if (rescale) {  // warp-uniform
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t v[32];
+            tc5::tmem_ld_32x32b_x32(to + 32 * c, v);
+            tc5::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tc5::tmem_st_32x32b_x32(to + 32 * c, v);
+          }
         }
         tc5::tmem_wait_st();
         bool zeroed = false;
