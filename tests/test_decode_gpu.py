@@ -72,6 +72,21 @@ SMALL = {
         num_kv_heads=1, head_size=576, head_size_v=512, block_size=64,
         v_aliases_k=True, kv_dtype=wl.FP8, scale_mode=wl.SCALE_TENSOR,
         softmax_scale=1 / 24, seed=9),
+    # the bf16 MLA head runs on the tensor cores (64-key chunks) at page
+    # sizes of a multiple of 8: partial chunks, several pages per chunk,
+    # one-page sequences and verify rows
+    "mla-12-b16": lambda: wl.make_workload(
+        "m12b16", seq_lens=[300, 65, 1], q_lens=[1, 1, 1], num_q_heads=12,
+        num_kv_heads=1, head_size=576, head_size_v=512, block_size=16,
+        v_aliases_k=True, softmax_scale=1 / 24, seed=16),
+    "mla-16-b32-verify": lambda: wl.make_workload(
+        "m16b32", seq_lens=[500, 129], q_lens=[2, 4], num_q_heads=16,
+        num_kv_heads=1, head_size=576, head_size_v=512, block_size=32,
+        v_aliases_k=True, softmax_scale=1 / 24, seed=17),
+    "mla-12-b8-hnd": lambda: wl.make_workload(
+        "m12b8", seq_lens=[200, 7], q_lens=[1, 1], num_q_heads=12,
+        num_kv_heads=1, head_size=576, head_size_v=512, block_size=8,
+        layout=wl.HND, v_aliases_k=True, softmax_scale=1 / 24, seed=18),
     "long-query-rows": lambda: wl.make_workload(
         "lq", seq_lens=[90, 50], q_lens=[20, 9], block_size=16, seed=10),
 }
