@@ -17,7 +17,9 @@ Also reported (``sub``): causal prefill TFLOP/s at 32,768 and 131,072 tokens
 and their cache writes, the 32,768-token prefill over an FP8 cache,
 speculative verify with an FP8 cache (16 x ~46K, q_len 4, 16 splits, 8
 padded rows) and the MLA-shaped decode (100K context, 12 and 16 heads, batch
-1 and 16).  Those are timed per launch with L2 flushed between launches.
+1 and 16).  Those are timed per launch with L2 flushed between launches;
+the decode sub-benchmarks also time the decode and its merge launched back
+to back as a step launches them (``step_ms``, one flush before the pair).
 The prefill loads K/V tiles with TMA multicast between the two CTAs of a
 cluster, which is for single-GPU jobs only: a run with more than one rank
 takes no prefill measurement (and ``--only prefill`` refuses to run).
@@ -329,8 +331,12 @@ def gpu_arm(args, ws, rank, local):
 
         def red_sink():  # the same merge with an attention sink per head
             pkv.splitkv_reduce(pok, plk, out=outk, sinks=sinks)
+        def step():  # the decode and its merge as a step launches them
+            dec()
+            red()
         md, _ = time_launches(dec, reps, 2, flush)
         mr, _ = time_launches(red, reps, 2, flush)
+        ms, _ = time_launches(step, reps, 2, flush)
         mrs, _ = time_launches(red_sink, reps, 2, flush)
         b = decode_bytes(wk)
         sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
@@ -338,7 +344,11 @@ def gpu_arm(args, ws, rank, local):
                      else "equal segments",
                      "bytes": b, "GBps": b / ((md + mr) * 1e-3) / 1e9,
                      "decode_kernel_GBps": b / (md * 1e-3) / 1e9,
+                     # each launch timed alone after an L2 flush
                      "frac_hbm": b / ((md + mr) * 1e-3) / 1e9 / hbm,
+                     # decode then merge back to back (programmatic launch,
+                     # partials still in L2), one L2 flush before the pair
+                     "step_ms": ms, "step_frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
                      "reduce_sink_ms": mrs, **wsub}
         del dwk, pok, plk, outk
         torch.cuda.empty_cache()
