@@ -315,7 +315,10 @@ int pkv_paged_attn_decode(const void *q, int num_q_heads, int num_tokens,
  * * block_size is required.  Other arguments, layouts and status codes as
  * in pkv_paged_attn_decode; PKV_EINVAL also for num_ranges < 0 or above
  * 2^24, or num_seqs * max_blocks_per_seq of 2^31 or more; PKV_EUNSUPPORTED
- * for more than 128 sequences (use pkv_paged_attn_decode).
+ * for more than 16384 sequences (use pkv_paged_attn_decode).  Up to 128
+ * sequences, every CTA reads all lengths once; beyond, a CTA reads them in
+ * chunks of 128 (their page counts first, then the chunk windows it needs),
+ * a few more dependent reads before its first copy.
  */
 int pkv_paged_attn_decode_balanced(const void *q, int num_q_heads, int num_tokens,
                                    const void *cache, const pkv_cache_desc *d,

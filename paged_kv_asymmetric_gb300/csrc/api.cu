@@ -484,7 +484,7 @@ int pkv_paged_attn_decode_balanced(const void* q, int num_q_heads, int num_token
   if (num_ranges < 0 || num_ranges > (1 << 24)) return PKV_EINVAL;
   // the batch's page line is counted in int
   if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX) return PKV_EINVAL;
-  if (num_seqs > pkv::kBalancedMaxSeqs) return PKV_EUNSUPPORTED;
+  if (num_seqs > pkv::kBalancedMaxSeqsWide) return PKV_EUNSUPPORTED;
   pkv::AttnParams p{};
   int sms = 0;
   bool launch = false;
@@ -552,7 +552,7 @@ int decode_fused_impl(const void* q, int num_q_heads, int num_tokens, const void
   if (balanced) {
     if (num_ranges > (1 << 24)) return PKV_EINVAL;
     if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX) return PKV_EINVAL;
-    if (num_seqs > pkv::kBalancedMaxSeqs) return PKV_EUNSUPPORTED;
+    if (num_seqs > pkv::kBalancedMaxSeqsWide) return PKV_EUNSUPPORTED;
   }
   pkv::AttnParams p{};
   int sms = 0;

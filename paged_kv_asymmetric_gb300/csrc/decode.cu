@@ -387,10 +387,12 @@ __device__ __forceinline__ void fused_finish(const AttnParams& p, const Unit& un
   named_barrier(1, NT);  // the weights are read before the buffer is reused
 }
 
-// BAL: the balanced-range unit list (split_ranges > 0) is compiled in; the
-// equal-segment form is its own instantiation, so that the code of one list
-// does not weigh on the other's register allocation.
-template <class C, bool BAL>
+// BAL: 0 equal segments; 1 balanced ranges (split_ranges > 0) over at most
+// MAXSORT sequences; 2 balanced ranges over more (a window of sequences).
+// Each unit list is its own instantiation, so that the code of one does not
+// weigh on another's (the window's bookkeeping slowed the headline batch by
+// 15 % when it was compiled into the same kernel).
+template <class C, int BAL>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map,
                   const __grid_constant__ CUtensorMap kv_map64, const AttnParams p,
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     // item's range, the item's head block, row group).  Items of one range
     // sit next to each other, so the CTAs that read the different heads of
     // the same pages run side by side.
-    constexpr bool balanced = BAL;
+    constexpr bool balanced = BAL != 0;
     int* gst = reinterpret_cast<int*>(smem + C::ORDER_OFF);  // [MAXSORT + 1]
     // query_start_loc[b] and seq_lens[b] of the lane registers (b uniform
     // over the warp; b == num_seqs gives the last query_start_loc entry)
@@ -513,109 +515,291 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
     int& qend = qend_;
     L4[0] = L4[1] = L4[2] = L4[3] = 0;
     Q4[0] = Q4[1] = Q4[2] = Q4[3] = 0;
-    if (balanced) {
-      // lane l takes sequences 4l .. 4l + 3: their page counts, then a warp
-      // scan of the lanes' sums gives every sequence's first global page
-      const int nb = p.num_seqs;
-      int P4[4], lsum = 0, lmax = 0;
-      qend = __ldg(p.query_start_loc + nb);
+    // A batch of more than MAXSORT sequences (BAL == 2) holds a window
+    // instead: the MAXSORT sequences of chunk wc (lane l: MAXSORT wc + 4l ..
+    // + 3) with their first global pages in G4, gst[] then holding every
+    // chunk's first global page and qend the first query token after the
+    // window.
+    int G4[4] = {0, 0, 0, 0};
+    const int nb = p.num_seqs;
+    constexpr bool wide = BAL == 2;
+    constexpr int WIN = C::MAXSORT;
+    const int nch = (nb + WIN - 1) / WIN;  // chunks (wide)
+    int wc = -1;                           // the window's chunk (wide)
+    auto npages = [&](int L) { return L > 0 ? (L + bs - 1) / bs : 0; };
+    // the window of chunk c (warp-uniform c): lengths, first query tokens,
+    // first global pages (gst[c] plus a warp scan inside the chunk)
+    auto load_window = [&](int c) {
+      wc = c;
+      int lsum = 0;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = 4 * lane + t;
+        const int i = WIN * c + 4 * lane + t;
         L4[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
         Q4[t] = i < nb ? __ldg(p.query_start_loc + i) : 0;
       }
+      qend = __ldg(p.query_start_loc + min(WIN * c + WIN, nb));
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int L = L4[t];
-        P4[t] = L > 0 ? (L + bs - 1) / bs : 0;
-        lsum += P4[t];
-        lmax = max(lmax, P4[t]);
-      }
+      for (int t = 0; t < 4; ++t) lsum += npages(L4[t]);
       int incl = lsum;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, d);
         if (lane >= d) incl += y;
       }
-      int g = incl - lsum;
+      int g = gst[c] + incl - lsum;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = 4 * lane + t;
-        if (i <= nb) gst[i] = g;
-        g += P4[t];
+        G4[t] = g;
+        g += npages(L4[t]);
       }
-      if (lane == 31 && nb == C::MAXSORT) gst[nb] = g;  // the entry past a full batch
+    };
+    // sequence b's first global page (0 <= b <= num_seqs; wide: b in the
+    // window or the first sequence after it), length and first query token
+    // (b == num_seqs, or past the window: the next first query token); b is
+    // uniform over the warp
+    auto gstart = [&](int b) -> int {
+      if (!wide) return gst[b];
+      const int i = b - WIN * wc;
+      return (i >= WIN || b >= nb) ? gst[wc + 1] : pick4(G4, i);
+    };
+    auto seq_Lb = [&](int b) { return wide ? pick4(L4_, b - WIN * wc) : seq_L(b); };
+    auto seq_qb = [&](int b) {
+      if (!wide) return seq_q(b);
+      const int i = b - WIN * wc;
+      return (i >= WIN || b >= nb) ? qend_ : pick4(Q4_, i);
+    };
+    if constexpr (!wide) {
+      if (balanced) {
+        // lane l takes sequences 4l .. 4l + 3: their page counts, then a warp
+        // scan of the lanes' sums gives every sequence's first global page
+        const int nb = p.num_seqs;
+        int P4[4], lsum = 0, lmax = 0;
+        qend = __ldg(p.query_start_loc + nb);
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, d));
-      const int64_t Ptot = __shfl_sync(0xffffffffu, incl, 31);
-      __syncwarp();
-      // R = max(ceil(Ptot / W), Rmin, 1): Rmin keeps every sequence within
-      // num_splits segments (one of P >= 2 pages meets at most
-      // floor((P - 2) / R) + 2 ranges)
-      const int64_t Rmin = p.num_splits == 1 ? Ptot
-                                             : (lmax > 2 ? lmax - 2 : 0) / (p.num_splits - 1) + 1;
-      bR = max(max((Ptot + p.split_ranges - 1) / p.split_ranges, Rmin), int64_t{1});
-      bnr = static_cast<int>((Ptot + bR - 1) / bR);
-      // segments past a sequence's last range hold no key: their lse is
-      // -inf, written here for the sequences b = blockIdx.x (mod gridDim.x)
-      for (int b = blockIdx.x; b < nb; b += gridDim.x) {
-        const int nseg = gst[b + 1] > gst[b]
-                             ? static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1)
-                             : 0;
-        const int q0 = seq_q(b);
-        const int rows = (seq_q(b + 1) - q0) * p.num_q_heads;
-        const int n = (p.num_splits - nseg) * rows;
-        for (int i = lane; i < n; i += 32) {
-          const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
-          p.partial_lse[(static_cast<int64_t>(sg) * T + q0) * p.num_q_heads + rr] = -INFINITY;
+        for (int t = 0; t < 4; ++t) {
+          const int i = 4 * lane + t;
+          L4[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+          Q4[t] = i < nb ? __ldg(p.query_start_loc + i) : 0;
         }
-        // fused merge: a sequence without keys has no unit to merge its
-        // rows, so they are written here (0, lse -inf)
-        if (p.fused && nseg == 0) {
-          for (int i = lane; i < rows * (C::DV / 2); i += 32) {
-            const int rr = i / (C::DV / 2), c2 = i - rr * (C::DV / 2);
-            reinterpret_cast<uint32_t*>(p.out + (static_cast<int64_t>(q0) * p.num_q_heads + rr) *
-                                                    C::DV)[c2] = 0u;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int L = L4[t];
+          P4[t] = L > 0 ? (L + bs - 1) / bs : 0;
+          lsum += P4[t];
+          lmax = max(lmax, P4[t]);
+        }
+        int incl = lsum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        int g = incl - lsum;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int i = 4 * lane + t;
+          if (i <= nb) gst[i] = g;
+          g += P4[t];
+        }
+        if (lane == 31 && nb == C::MAXSORT) gst[nb] = g;  // the entry past a full batch
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, d));
+        const int64_t Ptot = __shfl_sync(0xffffffffu, incl, 31);
+        __syncwarp();
+        // R = max(ceil(Ptot / W), Rmin, 1): Rmin keeps every sequence within
+        // num_splits segments (one of P >= 2 pages meets at most
+        // floor((P - 2) / R) + 2 ranges)
+        const int64_t Rmin = p.num_splits == 1 ? Ptot
+                                               : (lmax > 2 ? lmax - 2 : 0) / (p.num_splits - 1) + 1;
+        bR = max(max((Ptot + p.split_ranges - 1) / p.split_ranges, Rmin), int64_t{1});
+        bnr = static_cast<int>((Ptot + bR - 1) / bR);
+        // segments past a sequence's last range hold no key: their lse is
+        // -inf, written here for the sequences b = blockIdx.x (mod gridDim.x)
+        for (int b = blockIdx.x; b < nb; b += gridDim.x) {
+          const int nseg = gst[b + 1] > gst[b]
+                               ? static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1)
+                               : 0;
+          const int q0 = seq_q(b);
+          const int rows = (seq_q(b + 1) - q0) * p.num_q_heads;
+          const int n = (p.num_splits - nseg) * rows;
+          for (int i = lane; i < n; i += 32) {
+            const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
+            p.partial_lse[(static_cast<int64_t>(sg) * T + q0) * p.num_q_heads + rr] = -INFINITY;
           }
-          if (p.lse_out != nullptr)
-            for (int i = lane; i < rows; i += 32)
-              p.lse_out[static_cast<int64_t>(q0) * p.num_q_heads + i] = -INFINITY;
+          // fused merge: a sequence without keys has no unit to merge its
+          // rows, so they are written here (0, lse -inf)
+          if (p.fused && nseg == 0) {
+            for (int i = lane; i < rows * (C::DV / 2); i += 32) {
+              const int rr = i / (C::DV / 2), c2 = i - rr * (C::DV / 2);
+              reinterpret_cast<uint32_t*>(p.out + (static_cast<int64_t>(q0) * p.num_q_heads + rr) *
+                                                      C::DV)[c2] = 0u;
+            }
+            if (p.lse_out != nullptr)
+              for (int i = lane; i < rows; i += 32)
+                p.lse_out[static_cast<int64_t>(q0) * p.num_q_heads + i] = -INFINITY;
+          }
+        }
+      }
+    } else {
+      if (balanced) {
+        // every chunk's page count (the next chunk's lengths in flight while
+        // one is summed): gst[c] = the chunk's first global page
+        int lmax = 0;
+        int cur[4], run = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int i = 4 * lane + t;
+          cur[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+        }
+        for (int c = 0; c < nch; ++c) {
+          int nxt[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int i = WIN * (c + 1) + 4 * lane + t;
+            nxt[t] = i < nb ? __ldg(p.seq_lens + i) : 0;
+          }
+          int sum = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int P = npages(cur[t]);
+            sum += P;
+            lmax = max(lmax, P);
+          }
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+          if (lane == 0) gst[c] = run;
+          run += sum;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) cur[t] = nxt[t];
+        }
+        if (lane == 0) gst[nch] = run;
+        const int64_t Ptot = run;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, d));
+        __syncwarp();
+        // R = max(ceil(Ptot / W), Rmin, 1): Rmin keeps every sequence within
+        // num_splits segments (one of P >= 2 pages meets at most
+        // floor((P - 2) / R) + 2 ranges)
+        const int64_t Rmin = p.num_splits == 1 ? Ptot
+                                               : (lmax > 2 ? lmax - 2 : 0) / (p.num_splits - 1) + 1;
+        bR = max(max((Ptot + p.split_ranges - 1) / p.split_ranges, Rmin), int64_t{1});
+        bnr = static_cast<int>((Ptot + bR - 1) / bR);
+        // segments past a sequence's last range hold no key: their lse is
+        // -inf, written here for this CTA's block of consecutive sequences
+        auto fill_seq = [&](int b) {
+          const int g0 = gstart(b), g1 = gstart(b + 1);
+          const int nseg = g1 > g0 ? static_cast<int>((g1 - 1) / bR - g0 / bR + 1) : 0;
+          const int q0 = seq_qb(b);
+          const int rows = (seq_qb(b + 1) - q0) * p.num_q_heads;
+          const int n = (p.num_splits - nseg) * rows;
+          for (int i = lane; i < n; i += 32) {
+            const int sg = nseg + i / rows, rr = i - (i / rows) * rows;
+            p.partial_lse[(static_cast<int64_t>(sg) * T + q0) * p.num_q_heads + rr] = -INFINITY;
+          }
+          // fused merge: a sequence without keys has no unit to merge its
+          // rows, so they are written here (0, lse -inf)
+          if (p.fused && nseg == 0) {
+            for (int i = lane; i < rows * (C::DV / 2); i += 32) {
+              const int rr = i / (C::DV / 2), c2 = i - rr * (C::DV / 2);
+              reinterpret_cast<uint32_t*>(p.out + (static_cast<int64_t>(q0) * p.num_q_heads + rr) *
+                                                      C::DV)[c2] = 0u;
+            }
+            if (p.lse_out != nullptr)
+              for (int i = lane; i < rows; i += 32)
+                p.lse_out[static_cast<int64_t>(q0) * p.num_q_heads + i] = -INFINITY;
+          }
+        };
+        const int per = (nb + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+        const int b0 = static_cast<int>(blockIdx.x) * per, b1 = min(b0 + per, nb);
+        for (int b = b0; b < b1; ++b) {
+          if (b == b0 || b % WIN == 0) load_window(b / WIN);
+          fill_seq(b);
         }
       }
     }
     // work item, sequence, row group of the piece, the piece's pages
     int bi = blockIdx.x, bb = -1, bj = 0, bplo = 0, bphi = 0;
     int bL = 0, bq0 = 0, bq1 = 0;  // the piece's sequence: length, query_start_loc pair
+    // wide: the window that holds sequence b (warp-uniform b < num_seqs)
+    auto window_for = [&](int b) {
+      if (wide && b < nb && b / WIN != wc) load_window(b / WIN);
+    };
     // moves (bi, bb) to the next piece of a sequence inside the range of one
     // of this CTA's items; false when there is none
     auto next_piece = [&]() -> bool {
-      for (;;) {
-        if (bi >= bnr * us.HB) return false;
-        const int64_t r0 = static_cast<int64_t>(bi / us.HB) * bR;
-        const int64_t r1 = r0 + bR;
-        if (bb < 0) {  // the sequence holding global page r0: gst[bb] <= r0 < gst[bb + 1]
-          int lo = 0, hi = p.num_seqs - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (gst[mid + 1] > r0) hi = mid; else lo = mid + 1;
+      if constexpr (!wide) {
+        for (;;) {
+          if (bi >= bnr * us.HB) return false;
+          const int64_t r0 = static_cast<int64_t>(bi / us.HB) * bR;
+          const int64_t r1 = r0 + bR;
+          if (bb < 0) {  // the sequence holding global page r0: gst[bb] <= r0 < gst[bb + 1]
+            int lo = 0, hi = p.num_seqs - 1;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (gst[mid + 1] > r0) hi = mid; else lo = mid + 1;
+            }
+            bb = lo;
+          } else {
+            ++bb;
           }
-          bb = lo;
-        } else {
-          ++bb;
+          while (bb < p.num_seqs && gst[bb + 1] == gst[bb]) ++bb;  // no pages
+          if (bb < p.num_seqs && gst[bb] < r1) {
+            bplo = static_cast<int>(max(static_cast<int64_t>(gst[bb]), r0) - gst[bb]);
+            bphi = static_cast<int>(min(static_cast<int64_t>(gst[bb + 1]), r1) - gst[bb]);
+            bj = 0;
+            bL = seq_L(bb);
+            bq0 = seq_q(bb);
+            bq1 = seq_q(bb + 1);
+            return true;
+          }
+          bi += gridDim.x;
+          bb = -1;
         }
-        while (bb < p.num_seqs && gst[bb + 1] == gst[bb]) ++bb;  // no pages
-        if (bb < p.num_seqs && gst[bb] < r1) {
-          bplo = static_cast<int>(max(static_cast<int64_t>(gst[bb]), r0) - gst[bb]);
-          bphi = static_cast<int>(min(static_cast<int64_t>(gst[bb + 1]), r1) - gst[bb]);
-          bj = 0;
-          bL = seq_L(bb);
-          bq0 = seq_q(bb);
-          bq1 = seq_q(bb + 1);
-          return true;
+      } else {
+        for (;;) {
+          if (bi >= bnr * us.HB) return false;
+          const int64_t r0 = static_cast<int64_t>(bi / us.HB) * bR;
+          const int64_t r1 = r0 + bR;
+          if (bb < 0) {
+            // the chunk holding global page r0, then the one sequence of its
+            // window with pages around r0
+            int lo = 0, hi = nch - 1;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (gst[mid + 1] > r0) hi = mid; else lo = mid + 1;
+            }
+            if (lo != wc) load_window(lo);
+            int hit = -1;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int i = WIN * lo + 4 * lane + t;
+              const int P = npages(L4[t]);
+              if (i < nb && P > 0 && G4[t] <= r0 && r0 < G4[t] + P) hit = i;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+            bb = m ? __shfl_sync(0xffffffffu, hit, __ffs(m) - 1) : nb;
+          } else {
+            ++bb;
+            window_for(bb);
+          }
+          while (bb < nb && gstart(bb + 1) == gstart(bb)) {  // no pages
+            ++bb;
+            window_for(bb);
+          }
+          if (bb < nb && gstart(bb) < r1) {
+            const int g0 = gstart(bb), g1 = gstart(bb + 1);
+            bplo = static_cast<int>(max(static_cast<int64_t>(g0), r0) - g0);
+            bphi = static_cast<int>(min(static_cast<int64_t>(g1), r1) - g0);
+            bj = 0;
+            bL = seq_Lb(bb);
+            bq0 = seq_qb(bb);
+            bq1 = seq_qb(bb + 1);
+            return true;
+          }
+          bi += gridDim.x;
+          bb = -1;
         }
-        bi += gridDim.x;
-        bb = -1;
       }
     };
     bool bpiece = balanced && next_piece();
@@ -692,10 +876,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
       if (balanced) {
         if (!bpiece) return false;
         const int b = bb;
-        unit_params_pages<KPC>(p, b, bi % us.HB, bj,
-                               static_cast<int>(bi / us.HB - gst[b] / bR), bq0, bq1, bL, bplo,
-                               bphi, un);
-        un.nseg = static_cast<int>((gst[b + 1] - 1) / bR - gst[b] / bR + 1);
+        const int g0 = gstart(b), g1 = gstart(b + 1);
+        unit_params_pages<KPC>(p, b, bi % us.HB, bj, static_cast<int>(bi / us.HB - g0 / bR), bq0,
+                               bq1, bL, bplo, bphi, un);
+        un.nseg = static_cast<int>((g1 - 1) / bR - g0 / bR + 1);
         if (++bj == us.RG) bpiece = next_piece();
         if (un.s >= p.num_splits) {  // excluded by R >= Rmin; never written past the partials
           set_dev_error(p.err, PKV_EDEV_RANGE);
@@ -1870,10 +2054,11 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
 
 template <class C>
 cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
-  static int attr_set[2][64] = {{0}};
-  const bool bal = p.split_ranges > 0;
-  cudaError_t e = bal ? ensure_smem_attr(decode_kernel<C, true>, C::SMEM, attr_set[1])
-                      : ensure_smem_attr(decode_kernel<C, false>, C::SMEM, attr_set[0]);
+  static int attr_set[3][64] = {{0}};
+  const int bal = p.split_ranges <= 0 ? 0 : p.num_seqs <= kBalancedMaxSeqs ? 1 : 2;
+  cudaError_t e = bal == 2   ? ensure_smem_attr(decode_kernel<C, 2>, C::SMEM, attr_set[2])
+                  : bal == 1 ? ensure_smem_attr(decode_kernel<C, 1>, C::SMEM, attr_set[1])
+                             : ensure_smem_attr(decode_kernel<C, 0>, C::SMEM, attr_set[0]);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap kv_map;
   const int box_rows = box_rows_for(p.block_size, C::KPC);
@@ -1904,10 +2089,12 @@ cudaError_t launch_cfg(const AttnParams& p, int num_sms, cudaStream_t stream) {
                                   (p.num_kv_heads / C::HPC) * RG;
   const int64_t slots = static_cast<int64_t>(C::CTAS) * num_sms;
   const int grid = static_cast<int>(units < slots ? units : slots);
-  e = bal ? launch_pdl(decode_kernel<C, true>, grid, C::THREADS, C::SMEM, stream, kv_map,
-                       kv_map64, p, head_boxes)
-          : launch_pdl(decode_kernel<C, false>, grid, C::THREADS, C::SMEM, stream, kv_map,
-                       kv_map64, p, head_boxes);
+  e = bal == 2   ? launch_pdl(decode_kernel<C, 2>, grid, C::THREADS, C::SMEM, stream, kv_map,
+                              kv_map64, p, head_boxes)
+      : bal == 1 ? launch_pdl(decode_kernel<C, 1>, grid, C::THREADS, C::SMEM, stream, kv_map,
+                              kv_map64, p, head_boxes)
+                 : launch_pdl(decode_kernel<C, 0>, grid, C::THREADS, C::SMEM, stream, kv_map,
+                              kv_map64, p, head_boxes);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

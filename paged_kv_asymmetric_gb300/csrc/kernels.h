@@ -94,8 +94,11 @@ cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream)
 int decode_ctas_per_sm(const AttnParams& p);
 int decode_head_blocks(const AttnParams& p);
 // Balanced ranges keep every sequence's first page, length and query range
-// in shared memory: at most this many sequences per launch.
+// on chip for batches of up to kBalancedMaxSeqs sequences; larger batches
+// keep a window of that many sequences and every chunk's first page, so at
+// most kBalancedMaxSeqs chunks: kBalancedMaxSeqsWide sequences per launch.
 constexpr int kBalancedMaxSeqs = 128;
+constexpr int kBalancedMaxSeqsWide = kBalancedMaxSeqs * kBalancedMaxSeqs;
 bool decode_supported(int head_size, int head_size_v, int dtype);
 
 // sinks: nullable, one attention-sink logit per query head; row r takes

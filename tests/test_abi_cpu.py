@@ -167,7 +167,7 @@ def test_balanced_decode_rejects_bad_arguments(lib):
     d = _desc()
     assert _balanced(lib, d, W=-1) == pkv.EINVAL
     assert _balanced(lib, d, W=(1 << 24) + 1) == pkv.EINVAL
-    assert _balanced(lib, d, B=129) == pkv.EUNSUPPORTED      # more than 128 sequences
+    assert _balanced(lib, d, B=16385) == pkv.EUNSUPPORTED    # more than 128 x 128 sequences
     assert _balanced(lib, d, B=64, mb=1 << 26) == pkv.EINVAL  # page line past int
     assert _balanced(lib, d, S=0) == pkv.EINVAL
     assert _balanced(lib, d, po=None) == pkv.EINVAL
@@ -183,6 +183,7 @@ def test_balanced_shapes_pass_the_host_checks(lib):
     bf = _desc(num_blocks=4096)
     assert _balanced(lib, bf, T=32, B=32, mb=512, S=16) == pkv.ECUDA
     assert _balanced(lib, bf, W=152, T=128, B=128, mb=512, S=16) == pkv.ECUDA
+    assert _balanced(lib, bf, T=16384, B=16384, mb=8, S=16) == pkv.ECUDA   # wide batch
 
 
 def test_prefill_rejects_bad_arguments(lib):

@@ -91,12 +91,49 @@ def test_balanced_repeatable_and_many_ranges_per_cta():
     _check_partials(w, b[0], b[1], 64, W)
 
 
-def test_balanced_rejects_large_batches():
-    w = wl.make_workload("many", seq_lens=[20] * 129, q_lens=[1] * 129, seed=22)
+def _wide(name, n, seed, *, empty_chunk=False, **kw):
+    """n sequences (more than the 128 a CTA holds at once): lengths U[0, 300]
+    with every eleventh empty, q_len 1..4; with empty_chunk, sequences
+    128..255 (a whole chunk) are empty."""
+    g = np.random.default_rng(seed)
+    L = g.integers(0, 300, size=n, endpoint=True)
+    L[::11] = 0
+    if empty_chunk:
+        L[128:256] = 0
+    q = np.minimum(g.integers(1, 4, size=n, endpoint=True), np.maximum(L, 1))
+    return wl.make_workload(name, seq_lens=list(L), q_lens=list(q), seed=seed, **kw)
+
+
+WIDE = {
+    "129": lambda: _wide("w129", 129, 31),
+    "300-empty-chunk": lambda: _wide("w300", 300, 32, empty_chunk=True),
+    "256-fp8-b64": lambda: _wide("w256", 256, 33, kv_dtype=wl.FP8,
+                                 scale_mode=wl.SCALE_HEAD, block_size=64),
+}
+
+
+@pytest.mark.parametrize("name", list(WIDE))
+@pytest.mark.parametrize("S,W", [(16, 0), (16, 7), (4, 1000)])
+def test_balanced_wide_batches(name, S, W):
+    """More than 128 sequences: each CTA counts the pages chunk by chunk and
+    walks a window of 128 sequences; the segments are still the oracle's
+    balanced ranges (few ranges spanning many sequences and chunks, the
+    default, and more ranges than CTAs)."""
+    w = WIDE[name]()
     dw = wl.to_device(w)
-    with pytest.raises(pkv.PkvError) as e:
-        _decode(dw, 4, 0)
-    assert e.value.status == pkv.EUNSUPPORTED
+    gpu_path.write_all(dw)
+    We = W or pkv.decode_balanced_ranges(dw.cache)
+    po, pl, out, lse = _decode(dw, S, W)
+    _check_partials(w, po, pl, S, We)
+    _check_out(w, out, lse)
+    empty = gpu_path.tokens_of(w, [b for b in range(w.num_seqs) if w.seq_lens[b] == 0])
+    assert np.isneginf(gpu_path.host(pl)[:, empty]).all()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_rejects_bad_ranges():
+    w = WIDE["129"]()
+    dw = wl.to_device(w)
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_attn_decode_balanced(
             dw.q, dw.cache, dw.block_table, dw.seq_lens, dw.query_start_loc,
@@ -178,6 +215,23 @@ def test_balanced_fused_mixed_lengths_and_empty_sequences():
         out, lse = _fused(dw, S, W, ws)
         _check_out(w, out, lse)
         empty = gpu_path.tokens_of(w, [2, 4])
+        assert (gpu_path.host(out)[empty] == 0).all()
+        assert np.isneginf(gpu_path.host(lse)[empty]).all()
+    assert int(ws.abs().sum()) == 0
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+
+
+def test_balanced_fused_wide_batch():
+    """300 sequences with an empty chunk, merged in the launch: every row,
+    empty sequences 0 with lse -inf."""
+    w = WIDE["300-empty-chunk"]()
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    ws = _workspace(w)
+    for S, W in ((16, 0), (8, 7)):
+        out, lse = _fused(dw, S, W, ws)
+        _check_out(w, out, lse)
+        empty = gpu_path.tokens_of(w, [b for b in range(w.num_seqs) if w.seq_lens[b] == 0])
         assert (gpu_path.host(out)[empty] == 0).all()
         assert np.isneginf(gpu_path.host(lse)[empty]).all()
     assert int(ws.abs().sum()) == 0
