@@ -109,6 +109,14 @@ WIDE = {
     "300-empty-chunk": lambda: _wide("w300", 300, 32, empty_chunk=True),
     "256-fp8-b64": lambda: _wide("w256", 256, 33, kv_dtype=wl.FP8,
                                  scale_mode=wl.SCALE_HEAD, block_size=64),
+    # V before K in the row: the FP8 warp-MMA form
+    "200-fp8-vfirst": lambda: _wide("w200", 200, 34, kv_dtype=wl.FP8,
+                                    scale_mode=wl.SCALE_TENSOR, k_off=128, v_off=0,
+                                    row_elems=320),
+    # the MLA head (bf16, two CTAs per SM)
+    "150-mla": lambda: _wide("w150", 150, 35, num_q_heads=16, num_kv_heads=1,
+                             head_size=576, head_size_v=512, block_size=64,
+                             v_aliases_k=True, softmax_scale=1 / 24),
 }
 
 
