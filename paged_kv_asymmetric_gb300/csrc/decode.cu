@@ -2114,6 +2114,11 @@ using CfgFp8_192 = DecodeCfg<192, 128, true, 1, 1, 6, 64, 6, 2, 320>;
 using CfgFp8_192tc = DecodeCfg<192, 128, true, 1, 1, 1, 128, 3, 2, 320, false, 1, true>;
 // MLA 576 / 512: one latent head, 32 (bf16) or 64 (fp8) keys per chunk.
 using CfgBf16_576 = DecodeCfg<576, 512, false, 1, 4, 1, 32, 2, 1, 576, false, 2>;
+// the same with 16-key chunks in four ring slots, for short segments (a
+// unit of a few pages): its stream fills sooner (MLA batch 1 at 100K, six
+// pages a unit: 41.0 against 43.0 us), while long segments stream faster
+// in 32-key chunks (batch 16: 356 against 389 us)
+using CfgBf16_576s = DecodeCfg<576, 512, false, 1, 4, 1, 16, 4, 1, 576, false, 2>;
 using CfgFp8_576 = DecodeCfg<576, 512, true, 1, 4, 1, 64, 4, 2, 576>;
 
 }  // namespace
@@ -2123,6 +2128,21 @@ int decode_ctas_per_sm(const AttnParams& p) {
     return p.dtype == PKV_FP8_E4M3 ? CfgFp8_576::CTAS : CfgBf16_576::CTAS;
   return 1;
 }
+
+namespace {
+// Keys a segment holds at most, from what the host knows (the block-table
+// width, and the segment count or, for balanced ranges, the range count):
+// the MLA bf16 form takes 16-key chunks up to kShortSegKeys keys a unit.
+constexpr int64_t kShortSegKeys = 1024;
+bool short_segments(const AttnParams& p) {
+  const int64_t mb = p.max_blocks_per_seq;
+  const int64_t pages =
+      p.split_ranges > 0
+          ? (static_cast<int64_t>(p.num_seqs) * mb + p.split_ranges - 1) / p.split_ranges
+          : (mb + p.num_splits - 1) / p.num_splits;
+  return pages * p.block_size <= kShortSegKeys;
+}
+}  // namespace
 
 int decode_head_blocks(const AttnParams& p) {
   // four KV heads per unit only in the bf16 K192 form with Hkv % 4 == 0
@@ -2149,7 +2169,8 @@ cudaError_t launch_decode(const AttnParams& p, int num_sms, cudaStream_t stream)
   }
   if (p.head_size == 576 && p.head_size_v == 512)
     return fp8 ? launch_cfg<CfgFp8_576>(p, num_sms, stream)
-               : launch_cfg<CfgBf16_576>(p, num_sms, stream);
+               : short_segments(p) ? launch_cfg<CfgBf16_576s>(p, num_sms, stream)
+                                   : launch_cfg<CfgBf16_576>(p, num_sms, stream);
   return cudaErrorNotSupported;
 }
 
