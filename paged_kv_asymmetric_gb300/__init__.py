@@ -153,12 +153,23 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()  # ctypes passes the int as the c_void_p argument
+
+
+# The current device's current stream without the device lookups of
+# torch.cuda.current_stream(), which cost a few microseconds a call; torch's
+# public call is the fallback.
+_cuda_get_device = getattr(torch._C, "_cuda_getDevice", None)
+_cuda_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _cuda_get_device is not None and _cuda_raw_stream is not None and \
+            torch.cuda.is_initialized():
+        return _cuda_raw_stream(_cuda_get_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def make_desc(*, dtype=BF16, layout=NHD, num_blocks, block_size=16,
