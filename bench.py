@@ -111,7 +111,8 @@ def sub_plan(args, ws: int):
     if ws == 1 and not args.skip_prefill:
         plan += [("prefill", "prefill_32k", 32768),
                  ("prefill_fp8", "prefill_fp8_32k", 32768),
-                 ("prefill", "prefill_128k", 131072)]
+                 ("prefill", "prefill_128k", 131072),
+                 ("prefill_fp8", "prefill_fp8_128k", 131072)]
     plan.append(("verify", "verify_fp8", 16))
     plan += [("mla", f"mla_b{b}_h{h}", (b, h)) for b in (1, 16) for h in (12, 16)]
     return plan

@@ -1358,8 +1358,12 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
             l[j] += pr[j];
           }
           // ---- P^T (f16) for the B operand: [64-key atom][16 rows][128 B];
-          //      lane pairs swap values so each store holds two keys ----
+          //      lane pairs swap values so each store holds two keys.  The
+          //      even lane of a pair stores row j, the odd lane row j + 4:
+          //      rows 4 apart have complementary swizzled 16-byte chunks, so
+          //      the warp's 32 stores hit 32 different banks ----
           {
+            static_assert(RPT == 8, "P^T store pairs rows four apart");
             const uint32_t pb = pt_buf(c & 1u);
             const int k0 = kk & ~1;
             const bool odd = lane & 1;
@@ -1367,10 +1371,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
             const int kc = (k0 & 63) >> 3;
 #pragma unroll
             for (int j = 0; j < RPT / 2; ++j) {
-              const float send = odd ? pr[2 * j] : pr[2 * j + 1];
+              const float send = odd ? pr[j] : pr[j + RPT / 2];
               const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-              const int r = r0 + 2 * j + (odd ? 1 : 0);
-              const uint32_t val = odd ? pack_f16x2(recv, pr[2 * j + 1]) : pack_f16x2(pr[2 * j], recv);
+              const int r = r0 + j + (odd ? RPT / 2 : 0);
+              const uint32_t val = odd ? pack_f16x2(recv, pr[j + RPT / 2]) : pack_f16x2(pr[j], recv);
               asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(pbase + r * 128 + ((kc ^ (r & 7)) << 4)),
                            "r"(val) : "memory");
             }

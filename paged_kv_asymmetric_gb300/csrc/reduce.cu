@@ -11,8 +11,10 @@
 // a few MB next to the decode it follows, so its time is memory latency and
 // the number of dependent round trips, not bandwidth:
 //  * up to 32 splits (dv % 4 == 0): one warp per (row, 128 columns); lane s
-//    loads lse_s while every lane already has all S of its 16-byte partial
-//    loads in flight, so a row costs one round trip to memory;
+//    loads lse_s, and only the segments whose lse is finite have their
+//    16-byte partials loaded, all in flight together: two round trips, and
+//    no read of a partial the decode left unwritten (with balanced ranges
+//    most of a row's split slots are empty);
 //  * more splits: a CTA per (row, column block), the splits spread over
 //    its threads;
 //  * dv % 4 != 0: one warp per row, one column per lane.
@@ -76,10 +78,11 @@ __global__ void __launch_bounds__(256)
 }
 
 // Up to SB splits, dv % 4 == 0: warp g of the grid merges columns
-// [128 * cb, 128 * cb + 128) of row g / ncb (cb = g % ncb).  Every partial
-// of the row is loaded before its weight is known; a segment with weight 0
-// (lse -inf, or a weight that underflows) is skipped by a select, so an
-// unwritten partial never reaches the sum.  The weights pass from lane s to
+// [128 * cb, 128 * cb + 128) of row g / ncb (cb = g % ncb).  Lane s loads
+// lse_s; a ballot names the segments that saw a key, and only their
+// partials are loaded (an empty segment's partial was never written, and
+// reading it would cost HBM traffic for nothing).  A segment whose weight
+// underflows to 0 is skipped by a select.  The weights pass from lane s to
 // the others through shared memory.
 template <int SB>
 __global__ void __launch_bounds__(128)
@@ -101,12 +104,15 @@ __global__ void __launch_bounds__(128)
   const int c4 = static_cast<int>(g - static_cast<int64_t>(r) * ncb) * 32 + lane;
   const bool in = c4 < dv4;
   const float x = lane < S ? __ldg(plse + static_cast<int64_t>(lane) * rows + r) : -INFINITY;
+  // the segments with a visible key (bit s = segment s; none past S)
+  const uint32_t live = __ballot_sync(0xffffffffu, x != -INFINITY);
   const float4* po4 = reinterpret_cast<const float4*>(po);
   float4 v[SB];
 #pragma unroll
   for (int s = 0; s < SB; ++s)
-    v[s] = (s < S && in) ? __ldg(po4 + (static_cast<int64_t>(s) * rows + r) * dv4 + c4)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[s] = (((live >> s) & 1u) && in)
+               ? __ldg(po4 + (static_cast<int64_t>(s) * rows + r) * dv4 + c4)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = x;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));

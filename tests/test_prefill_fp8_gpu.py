@@ -152,3 +152,35 @@ def test_fp8_prefill_32k_sampled():
     assert len(toks) * 16 >= 2048
     _run(w, tokens=toks, seqs=[0])
     _run(w, tokens=toks, seqs=[0], two_pass=True)
+
+
+def test_fp8_prefill_131k_sampled():
+    """The 131,072-token prefill over an FP8 cache with per-head scales, both
+    forms (widened in the kernel, and two-pass through the workspace): the
+    first and last dealt units, the middle ones, tile edges and a random
+    spread, every head, against the oracle.  Sampled rows are gathered on
+    the device, so only they come back to the host."""
+    from tests.test_prefill_gpu import prefill_sample_tokens
+    n = 131072
+    w = wl.make_workload(f"prefill-{n}-fp8", seq_lens=[n], q_lens=[n],
+                         kv_dtype=wl.FP8, scale_mode=H, seed=0)
+    units = [0, 1, 2, 511, 512, 1000, 1021, 1022, 1023]
+    toks = prefill_sample_tokens(n, units, 16, seed=2)
+    assert len(toks) * 16 >= 1024
+    dw = wl.to_device(w)
+    gpu_path.write_all(dw)
+    gpu_path.device_error()
+    idx = torch.from_numpy(toks.astype(np.int64)).cuda()
+    n_ws = pkv.prefill_fp8_workspace_bytes(w.num_seqs, dw.block_table.shape[1], dw.cache)
+    got = []
+    for ws in (None, torch.empty(n_ws, dtype=torch.uint8, device="cuda")):
+        out = pkv.paged_attn_prefill(dw.q, dw.cache, dw.block_table, dw.seq_lens,
+                                     dw.query_start_loc, w.softmax_scale,
+                                     k_scale=dw.k_scale, v_scale=dw.v_scale, workspace=ws)
+        got.append(gpu_path.host(out[idx]))
+        del out
+    torch.cuda.synchronize()
+    assert gpu_path.device_error() == pkv.EDEV_NONE
+    o, _ = gpu_path.oracle_rows(w, tokens=toks, seqs=[0])
+    for g in got:
+        refs.assert_close(g, o, **gpu_path.FP8_TOL, what=w.name)

@@ -53,6 +53,21 @@ CASES = {
         seed=8),
     "scaled-scores": lambda: wl.make_workload(
         "hot", seq_lens=[400], q_lens=[400], softmax_scale=0.5, seed=9),
+    # page-grouped boxes with other geometries: 8- and 32-key pages (NHD),
+    # V ahead of K in the row
+    "block8-nhd": lambda: wl.make_workload(
+        "b8n", seq_lens=[150, 40], q_lens=[150, 17], block_size=8, seed=10),
+    "block32": lambda: wl.make_workload(
+        "b32", seq_lens=[333], q_lens=[333], block_size=32, seed=11),
+    "v-first-row": lambda: wl.make_workload(
+        "vf", seq_lens=[260, 31], q_lens=[260, 31], k_off=128, v_off=0, seed=12),
+    # rows that do not split into 64-column slabs (V at column 200 of 328):
+    # one box per 64-column slab and page
+    "padded-row": lambda: wl.make_workload(
+        "pad", seq_lens=[300, 45], q_lens=[300, 45], row_elems=328, v_off=200, seed=13),
+    "padded-row-hnd-b64": lambda: wl.make_workload(
+        "padh", seq_lens=[200], q_lens=[200], row_elems=336, v_off=200, block_size=64,
+        layout=wl.HND, seed=14),
 }
 
 
