@@ -19,7 +19,11 @@ speculative verify with an FP8 cache (16 x ~46K, q_len 4, 16 splits, 8
 padded rows) and the MLA-shaped decode (100K context, 12 and 16 heads, batch
 1 and 16).  Those are timed per launch with L2 flushed between launches;
 the decode sub-benchmarks also time the decode and its merge launched back
-to back as a step launches them (``step_ms``, one flush before the pair).
+to back as a step launches them (``step_ms``, one flush before the pair),
+and, where the KV cache is larger than L2 (verify, MLA batch 16), a loop of
+such steps with no flush and no event inside it (``loop_step_ms``), the
+steps alternating between two copies of the cache so that no step can find
+the previous step's pages in L2.
 The prefill loads K/V tiles with TMA multicast between the two CTAs of a
 cluster, which is for single-GPU jobs only: a run with more than one rank
 takes no prefill measurement (and ``--only prefill`` refuses to run).
@@ -313,14 +317,15 @@ def gpu_arm(args, ws, rank, local):
         plk = torch.empty(splits, Tk, Hk, dtype=torch.float32, device=dev)
         outk = torch.empty(Tk, Hk, dvk, dtype=torch.bfloat16, device=dev)
 
-        def dec():
+        def dec(cache=None):
+            cache = dwk.cache if cache is None else cache
             if balanced:
                 pkv.paged_attn_decode_balanced(
-                    dwk.q, dwk.cache, dwk.block_table, dwk.seq_lens, dwk.query_start_loc,
+                    dwk.q, cache, dwk.block_table, dwk.seq_lens, dwk.query_start_loc,
                     wk.softmax_scale, wk.max_query_len, splits, 0, partial_o=pok,
                     partial_lse=plk, k_scale=dwk.k_scale, v_scale=dwk.v_scale)
             else:
-                pkv.paged_attn_decode(dwk.q, dwk.cache, dwk.block_table,
+                pkv.paged_attn_decode(dwk.q, cache, dwk.block_table,
                                       dwk.seq_lens, dwk.query_start_loc,
                                       wk.softmax_scale, wk.max_query_len, splits,
                                       partial_o=pok, partial_lse=plk,
@@ -340,6 +345,30 @@ def gpu_arm(args, ws, rank, local):
         ms, _ = time_launches(step, reps, 2, flush)
         mrs, _ = time_launches(red_sink, reps, 2, flush)
         b = decode_bytes(wk)
+        loop = {}
+        cache_bytes = dwk.cache.data.numel() * dwk.cache.data.element_size()
+        if cache_bytes >= L2_FLUSH_BYTES:
+            # steps back to back (inputs larger than L2): decode + merge, the
+            # decode reading two copies of the cache in turn
+            caches = (dwk.cache, pkv.Cache(dwk.cache.data.clone(), dwk.cache.desc))
+            n_loop = 4 * max(10, reps)
+            for i in range(4):
+                dec(caches[i & 1])
+                red()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for i in range(n_loop):
+                dec(caches[i & 1])
+                red()
+            e1.record()
+            e1.synchronize()
+            ml = e0.elapsed_time(e1) / n_loop
+            loop = {"loop_step_ms": ml, "loop_step_frac_hbm": b / (ml * 1e-3) / 1e9 / hbm,
+                    "loop_steps": n_loop}
+            del caches
+
         sub[name] = {"decode_ms": md, "reduce_ms": mr, "splits": splits,
                      "segments": "balanced ranges (at most splits)" if balanced
                      else "equal segments",
@@ -350,7 +379,7 @@ def gpu_arm(args, ws, rank, local):
                      # decode then merge back to back (programmatic launch,
                      # partials still in L2), one L2 flush before the pair
                      "step_ms": ms, "step_frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
-                     "reduce_sink_ms": mrs, **wsub}
+                     **loop, "reduce_sink_ms": mrs, **wsub}
         del dwk, pok, plk, outk
         torch.cuda.empty_cache()
 
