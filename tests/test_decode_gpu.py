@@ -72,9 +72,8 @@ SMALL = {
         num_kv_heads=1, head_size=576, head_size_v=512, block_size=64,
         v_aliases_k=True, kv_dtype=wl.FP8, scale_mode=wl.SCALE_TENSOR,
         softmax_scale=1 / 24, seed=9),
-    # the bf16 MLA head runs on the tensor cores (64-key chunks) at page
-    # sizes of a multiple of 8: partial chunks, several pages per chunk,
-    # one-page sequences and verify rows
+    # the MLA head at other page sizes: partial chunks, several pages per
+    # chunk, one-page sequences and verify rows
     "mla-12-b16": lambda: wl.make_workload(
         "m12b16", seq_lens=[300, 65, 1], q_lens=[1, 1, 1], num_q_heads=12,
         num_kv_heads=1, head_size=576, head_size_v=512, block_size=16,
@@ -89,6 +88,13 @@ SMALL = {
         layout=wl.HND, v_aliases_k=True, softmax_scale=1 / 24, seed=18),
     "long-query-rows": lambda: wl.make_workload(
         "lq", seq_lens=[90, 50], q_lens=[20, 9], block_size=16, seed=10),
+    # the longest query the decode takes (64 tokens: 256 rows of a KV head,
+    # 16 row groups), bf16 and on the FP8 tensor-core form
+    "max-query-rows": lambda: wl.make_workload(
+        "mq", seq_lens=[200, 64], q_lens=[64, 64], block_size=16, seed=19),
+    "max-query-rows-fp8": lambda: wl.make_workload(
+        "mq8", seq_lens=[300, 70], q_lens=[64, 64], block_size=64, kv_dtype=wl.FP8,
+        scale_mode=wl.SCALE_HEAD, seed=20),
 }
 
 
