@@ -1859,18 +1859,21 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS)
               for (int e = 0; e < 4; ++e) s[t][e] += s2[t][e];
           }
           if constexpr (WG > 1) {  // sum the K-slice partial scores of the group
+            // a warp's block holds its two key tiles one after the other,
+            // each as 32 lanes x 16 contiguous bytes, so every 16-byte store
+            // and load of the warp is free of bank conflicts
             const int buf = xk & 1u;
-            float* mine = sbuf + (buf * WG + wig) * 32 * 8 + lane * 8;
+            float* mine = sbuf + (buf * WG + wig) * 32 * 8 + lane * 4;
             *reinterpret_cast<float4*>(mine) = make_float4(s[0][0], s[0][1], s[0][2], s[0][3]);
-            *reinterpret_cast<float4*>(mine + 4) = make_float4(s[1][0], s[1][1], s[1][2], s[1][3]);
+            *reinterpret_cast<float4*>(mine + 128) = make_float4(s[1][0], s[1][1], s[1][2], s[1][3]);
             group_sync();
 #pragma unroll
             for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < WG; ++w2) {
-              const float* src = sbuf + (buf * WG + w2) * 32 * 8 + lane * 8;
+              const float* src = sbuf + (buf * WG + w2) * 32 * 8 + lane * 4;
               const float4 x = *reinterpret_cast<const float4*>(src);
-              const float4 y = *reinterpret_cast<const float4*>(src + 4);
+              const float4 y = *reinterpret_cast<const float4*>(src + 128);
               s[0][0] += x.x; s[0][1] += x.y; s[0][2] += x.z; s[0][3] += x.w;
               s[1][0] += y.x; s[1][1] += y.y; s[1][2] += y.z; s[1][3] += y.w;
             }
