@@ -103,6 +103,53 @@ inline bool make_cache_tmap_heads(CUtensorMap* map, const void* cache, int dtype
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 5-D map over a bf16 cache whose rows split into 64-column slabs
+// (row_elems a multiple of 64), for page-grouped loads: coordinates (col
+// 0..63 of a slab, key 0..7 of an 8-key group, slab, group within the page,
+// page), with the KV head folded into the slab index (NHD: a head's row is
+// the next R / 64 slabs) or into the page index (HND: page * H + head).  A
+// box of (64, 8, nslab, box_rows / 8, 1) holds the nslab slabs of
+// box_rows keys of one page and head and lands in shared memory as
+// [8-key group][slab][8 keys][128 bytes], 128-byte swizzled.  The strides do
+// not increase (a key's stride exceeds a slab's), which the encoder accepts
+// (the decode's head-block maps have the same property).
+inline bool make_cache_tmap_groups(CUtensorMap* map, const void* cache, int layout,
+                                   int num_blocks, int block_size, int num_kv_heads,
+                                   int row_elems, int nslab, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encode_fn();
+  if (encode == nullptr) return false;
+  if (row_elems % 64 != 0 || block_size % 8 != 0 || box_rows % 8 != 0) return false;
+  const cuuint64_t R = static_cast<cuuint64_t>(row_elems);
+  const cuuint64_t H = static_cast<cuuint64_t>(num_kv_heads);
+  const cuuint64_t B = static_cast<cuuint64_t>(block_size);
+  const cuuint64_t NB = static_cast<cuuint64_t>(num_blocks);
+  cuuint64_t dims[5], strides[4];
+  dims[0] = 64;
+  dims[1] = 8;
+  dims[3] = B / 8;
+  strides[1] = 128;
+  if (layout == PKV_NHD) {  // [blk][bs][H][R]
+    dims[2] = H * R / 64;
+    dims[4] = NB;
+    strides[0] = H * R * 2;
+    strides[2] = 8 * H * R * 2;
+    strides[3] = B * H * R * 2;
+  } else {                  // [blk][H][bs][R]
+    dims[2] = R / 64;
+    dims[4] = NB * H;
+    strides[0] = R * 2;
+    strides[2] = 8 * R * 2;
+    strides[3] = B * R * 2;
+  }
+  const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(nslab),
+                             static_cast<cuuint32_t>(box_rows / 8), 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Sets the dynamic shared-memory limit of `fn` once per device.
 template <class F>
 inline cudaError_t ensure_smem_attr(F* fn, int bytes, int* done) {
