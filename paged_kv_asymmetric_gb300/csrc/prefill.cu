@@ -15,16 +15,18 @@
 //    two 128-row query tiles of one KV head (tiles A and B); a tile is 128 / G
 //    consecutive tokens x the G query heads that share the KV head (GQA
 //    packing).  The two CTAs of a cluster take adjacent items of the same
-//    sequence and KV head and walk the same key tiles: each K/V box is read
-//    from L2 once, by one of them, and multicast into both shared memories,
-//    so a K/V tile feeds 4 x 128 query rows.  (Without this the loads alone
-//    ran at ~3.6 TB/s from L2 and bounded the kernel.)  Units are numbered
-//    longest-first and dealt to the clusters in alternating directions.
+//    sequence and KV head and walk the same key tiles: with slab fills each
+//    K/V box is read from L2 once, by one of them, and multicast into both
+//    shared memories, so a K/V tile feeds 4 x 128 query rows.  (Without this
+//    the slab boxes alone ran at ~3.6 TB/s from L2 and bounded the kernel.)
+//    Units are numbered longest-first and dealt to the clusters in
+//    alternating directions.
 //  * Warp roles: warp 0 issues TMA loads (the two Q tiles as 64-column slabs;
 //    K and V pages as 64-column boxes of one page each into 128-key slabs of
-//    an 8-slab ring, half of each slab's boxes per CTA; a slot is refilled
-//    once the MMAs of both CTAs have read it; page ids prefetched two tiles
-//    ahead by all lanes),
+//    an 8-slab ring, half of each slab's boxes per CTA, a slot refilled once
+//    the MMAs of both CTAs have read it; or, for small pages, page-grouped
+//    boxes into part slots, below; page ids prefetched two tiles ahead by
+//    all lanes),
 //    warp 1 issues tcgen05.mma from one thread, warps 4..7 run the softmax
 //    of tile A and warps 8..11 that of tile B, one thread per query row.
 //  * Tensor memory holds S and O of both tiles (4 x 128 columns).  The
