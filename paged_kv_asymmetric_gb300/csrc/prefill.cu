@@ -24,9 +24,8 @@
 //  * Warp roles: warp 0 issues TMA loads (the two Q tiles as 64-column slabs;
 //    K and V pages as 64-column boxes of one page each into 128-key slabs of
 //    an 8-slab ring, half of each slab's boxes per CTA, a slot refilled once
-//    the MMAs of both CTAs have read it; or, for small pages, page-grouped
-//    boxes into part slots, below; page ids prefetched two tiles ahead by
-//    all lanes),
+//    the MMAs of both CTAs have read it; or page-grouped boxes into part
+//    slots, below; page ids prefetched two tiles ahead by all lanes),
 //    warp 1 issues tcgen05.mma from one thread, warps 4..7 run the softmax
 //    of tile A and warps 8..11 that of tile B, one thread per query row.
 //  * Tensor memory holds S and O of both tiles (4 x 128 columns).  The
@@ -39,19 +38,19 @@
 //    Issue order: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
 //    A commit after S_X(j+1) also covers PV_X(j), so when the softmax sees
 //    S_X(j+1) ready, P_X(j) has been consumed and O_X is stable.
-//  * Small pages (8 or 16 keys; bf16 caches whose rows split into 64-column
-//    slabs): page-grouped fills.  A key tile's K part (three slabs) and V
-//    part (two) are laid out as [8-key group][slab][8 keys][128 B], so one
-//    5-D TMA box per page brings all of a part's columns for that page's
-//    keys: 16 boxes per 128-key tile of 16-key pages instead of 40, where the
-//    rate of boxes had paced the loads.  The ring then holds three fixed part
-//    slots: two K slots taken by alternate tiles (a tile's K is loaded while
-//    the previous one is still read) and one V slot.  The producer issues the
-//    K of tile j + 1 before the V of tile j, and each CTA loads its own parts
-//    (per-CTA boxes stream faster than multicast ones at this size).  The
-//    MMAs step over a part's key groups at a 3 KB (K) or 2 KB (V) stride.
-//    Larger pages, other row layouts and FP8 caches fill one 64-column slab
-//    at a time into the 8-slab ring, multicast to both CTAs of the cluster.
+//  * bf16 caches whose rows split into 64-column slabs: page-grouped fills.
+//    A key tile's K part (three slabs) and V part (two) are laid out as
+//    [8-key group][slab][8 keys][128 B], so one 5-D TMA box per 16 keys of a
+//    page brings all of a part's columns for them: 16 boxes per 128-key tile
+//    instead of 40 at 16-key pages.  The ring holds fixed part slots: two K
+//    slots taken by alternate tiles (a tile's K is loaded while the previous
+//    one is still read) and a V slot of two 64-key halves with their own
+//    barriers (the next tile's first half loads while the MMAs still read
+//    the second, and P.V starts on the first half before the second lands).
+//    The producer issues the K of tile j + 1 before the V of tile j, and each
+//    CTA loads its own parts.  The MMAs step over a part's key groups at a
+//    3 KB (K) or 2 KB (V) stride.  Other row layouts and FP8 caches fill one
+//    64-column slab at a time into the 8-slab ring, multicast to both CTAs.
 //  * Online softmax with a lazy rescale: the exponent base moves (and O and
 //    the running sum are rescaled in place) only when a row maximum grows by
 //    more than 2^8, decided per warp; the result is the same up to rounding.
@@ -125,13 +124,15 @@ __device__ __forceinline__ uint32_t v_fill(uint32_t fbase, int j, int h) {
   return fbase + FILLS_PER_TILE * j + (v_first(fbase, j) ? 0 : KSLABS) + h;
 }
 
-// Page-grouped fills use the ring as three fixed part slots: K parts of
-// tiles alternate between slabs 0..2 and 3..5 (a K part is loaded while the
-// other is still read), and every tile's V part takes slabs 6..7.  Tile t
-// (counted over the CTA's items) uses K slot t & 1, its full and empty
-// barriers being those of the slot's first slab; its n-th use is phase
-// n & 1 (K: n = t >> 1; V: n = t).  Each CTA loads its own parts, so a slot
-// is free once this CTA's MMAs have read it.
+// Page-grouped fills use the ring as fixed part slots: K parts of tiles
+// alternate between slabs 0..2 and 3..5 (a K part is loaded while the other
+// is still read), and every tile's V part takes slabs 6..7, one slab per
+// 64-key half with its own barriers (the next tile's first half loads while
+// the MMAs still read the second, and P.V starts on the first half before
+// the second lands).  Tile t (counted over the CTA's items) uses K slot
+// t & 1, whose barriers are those of its first slab; a slot's n-th use is
+// phase n & 1 (K: n = t >> 1; V: n = t).  Each CTA loads its own parts, so
+// a slot is free once this CTA's MMAs have read it.
 __device__ __forceinline__ uint32_t kslot_slab(uint32_t t) { return (t & 1u) * KSLABS; }
 constexpr uint32_t VSLOT_SLAB = 2 * KSLABS;
 static_assert(VSLOT_SLAB + VSLABS <= NSLAB, "three part slots in the ring");
@@ -306,7 +307,11 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int bs = p.block_size;
-  const int box_rows = bs < BN ? bs : BN;
+  // rows of a K/V box: a page, or 128 keys of it (slab fills) or 16 keys of
+  // it (page-grouped fills: eight or more boxes a part in flight stream
+  // faster than fewer larger ones, and a V part's two key halves each get
+  // whole boxes)
+  const int box_rows = PG ? (bs < 16 ? bs : 16) : (bs < BN ? bs : BN);
   const int nbox = BN / box_rows;
 
   // Registers: the bf16 block is launched with 384 x 168; the control
@@ -369,10 +374,11 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
     // page-grouped fills: tile t's K part (kv_map, slot t & 1) or V part
     // (v_map, the V slot): one box per page, each CTA loading its own, the
     // slot's previous use read by this CTA's MMAs first
-    uint32_t tk = 0, tv = 0;  // K and V parts issued
-    auto fill_part = [&](const Item& it, int kt, bool is_v, int pid) -> bool {
+    uint32_t tk = 0, tv = 0;  // K parts and V parts (both halves) issued
+    // vh: the 64-key half of a V part (its boxes and its slab)
+    auto fill_part = [&](const Item& it, int kt, bool is_v, int pid, int vh) -> bool {
       const uint32_t t = is_v ? tv : tk;
-      const uint32_t slab = is_v ? VSLOT_SLAB : kslot_slab(t);
+      const uint32_t slab = is_v ? VSLOT_SLAB + vh : kslot_slab(t);
       const uint32_t use = is_v ? t : t >> 1;
       bool w = true;
       if (lane == 0)
@@ -381,11 +387,17 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
       const int nsl = is_v ? VSLABS : KSLABS;
       const int lim = it.L - kt * BN;
       const int nb = min(nbox, (lim + box_rows - 1) / box_rows);
+      // this fill's boxes: all of a K part, one half of a V part (none when
+      // the sequence ends in the first half: the phase then completes
+      // with no bytes)
+      const int b0 = is_v ? vh * (nbox / 2) : 0;
+      const int b1 = min(nb, is_v ? b0 + nbox / 2 : nbox);
       const uint32_t full = bar(B_SLAB_FULL0 + slab);
       if (lane == 0)
-        tc5::mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb * box_rows * nsl * 128));
+        tc5::mbar_arrive_expect_tx(
+            full, static_cast<uint32_t>(max(0, b1 - b0) * box_rows * nsl * 128));
       __syncwarp();
-      if (lane < nb) {
+      if (lane >= b0 && lane < b1) {
         const int key0 = kt * BN + lane * box_rows;
         const int off = key0 % bs;
         int page = pid;
@@ -393,7 +405,7 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           set_dev_error(p.err, PKV_EDEV_RANGE);
           page = p.num_blocks;  // out-of-range box: TMA fills zeros
         }
-        const uint32_t dst = sbase + RING_OFF + slab * SLAB +
+        const uint32_t dst = sbase + RING_OFF + (is_v ? VSLOT_SLAB : slab) * SLAB +
                              static_cast<uint32_t>(lane * box_rows * nsl * 128);
         int cs = (is_v ? p.v_off : p.k_off) / 64, pg = page;
         if (p.layout == PKV_NHD)
@@ -402,7 +414,10 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           pg = page * p.num_kv_heads + it.g;
         tc5::tma_load_5d(dst, is_v ? &v_map : &kv_map, 0, 0, cs, off / 8, pg, full);
       }
-      if (is_v) ++tv; else ++tk;
+      if (!is_v)
+        ++tk;
+      else if (vh == 1)
+        ++tv;
       return true;
     };
     for (int k = 0; ok; ++k) {
@@ -426,12 +441,13 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
       ++qi;
       // page-grouped: K runs one tile ahead of V (K of tile j + 1 is issued
       // before V of tile j, as its slot frees earlier)
-      if constexpr (PG) ok = fill_part(it, 0, false, pid0);
+      if constexpr (PG) ok = fill_part(it, 0, false, pid0, 0);
       for (int j = 0; j < it.ntiles && ok; ++j) {
         const int pid2 = load_pid(it, j + 2);  // prefetch
         if constexpr (PG) {
-          if (j + 1 < it.ntiles) ok = fill_part(it, j + 1, false, pid1);
-          if (ok) ok = fill_part(it, j, true, pid0);
+          if (j + 1 < it.ntiles) ok = fill_part(it, j + 1, false, pid1, 0);
+          if (ok) ok = fill_part(it, j, true, pid0, 0);
+          if (ok) ok = fill_part(it, j, true, pid0, 1);
         } else {
           const bool vf = v_first(f, 0);
           for (int h = 0; h < VSLABS && ok && vf; ++h) ok = fill_slab(it, j, p.v_off + 64 * h, pid0);
@@ -450,8 +466,9 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           tc5::mbar_wait(bar(B_SLAB_FULL0 + kslot_slab(t)), (t >> 1) & 1u, abort_flag, p.err,
                          /*honor_abort=*/false);
         if (tv > 0)
-          tc5::mbar_wait(bar(B_SLAB_FULL0 + VSLOT_SLAB), (tv - 1) & 1u, abort_flag, p.err,
-                         /*honor_abort=*/false);
+          for (int h = 0; h < 2; ++h)
+            tc5::mbar_wait(bar(B_SLAB_FULL0 + VSLOT_SLAB + h), (tv - 1) & 1u, abort_flag, p.err,
+                           /*honor_abort=*/false);
       }
       for (uint32_t k = f > NSLAB ? f - NSLAB : 0; k < f; ++k)
         tc5::mbar_wait(bar(B_SLAB_FULL0 + k % NSLAB), (k / NSLAB) & 1u, abort_flag,
@@ -499,10 +516,12 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
     // O_x += P_x V_j: N = 128 over V's two 64-column slabs (the leading byte
     // offset steps from one to the other: the next slab, or 1 KB on in a
     // page-grouped part), K = 16 keys (two 8-key groups) a step
-    auto issue_pv_at = [&](int x, uint32_t va, uint32_t lbo, uint32_t vgs, bool first) {
+    // (keys 16 k0 .. 16 k1 - 1 of the tile)
+    auto issue_pv_at = [&](int x, uint32_t va, uint32_t lbo, uint32_t vgs, bool first, int k0,
+                           int k1) {
       tc5::tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
+      for (int kk = k0; kk < k1; ++kk)
         tc5::mma_f16_ts(tmem + tm_o(x), tmem + tm_s(x) + 8 * kk,
                         tc5::sdesc_sw128(va + kk * 2 * vgs, lbo, vgs), idesc_pv,
                         (!first || kk > 0) ? 1u : 0u);
@@ -531,14 +550,19 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t t = t0 + static_cast<uint32_t>(j);
           for (int x = 0; x < 2 && ok; ++x) {
-            if (x == 0) wait(B_SLAB_FULL0 + VSLOT_SLAB, t & 1u);
+            if (x == 0) wait(B_SLAB_FULL0 + VSLOT_SLAB, t & 1u);  // V keys 0..63
             wait(B_PFULL0 + x, pc[x] & 1u);
             if (j == 0) wait(B_OFREE0 + x, (qi & 1u) ^ 1u);
             if (!ok) break;
             ++pc[x];
-            issue_pv_at(x, vaddr, 1024u, VGROUP, j == 0);
-            if (j == n - 1) tc5::mma_commit(bar(B_ODONE0 + x));
+            issue_pv_at(x, vaddr, 1024u, VGROUP, j == 0, 0, BN / 32);
+            // the first half is free once P.V_B has read it
             if (x == 1) tc5::mma_commit(bar(B_SLAB_EMPTY0 + VSLOT_SLAB));
+            if (x == 0) wait(B_SLAB_FULL0 + VSLOT_SLAB + 1, t & 1u);  // V keys 64..127
+            if (!ok) break;
+            issue_pv_at(x, vaddr, 1024u, VGROUP, j == 0, BN / 32, BN / 16);
+            if (j == n - 1) tc5::mma_commit(bar(B_ODONE0 + x));
+            if (x == 1) tc5::mma_commit(bar(B_SLAB_EMPTY0 + VSLOT_SLAB + 1));
             if (j + 1 < n) {
               if (x == 0) kwait(t + 1);
               if (!ok) break;
@@ -570,7 +594,7 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           if (!ok) break;
           ++pc[x];
           issue_pv_at(x, slab_addr(v_fill(fbase, j, 0)), static_cast<uint32_t>(SLAB), 1024u,
-                      j == 0);
+                      j == 0, 0, BN / 16);
           if (j == n - 1) tc5::mma_commit(bar(B_ODONE0 + x));
           if (x == 1)
             for (int h = 0; h < VSLABS; ++h)
@@ -778,8 +802,8 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
           const uint32_t tv = tcnt + static_cast<uint32_t>(j);  // page-grouped tile
           for (int h = 0; h < VSLABS && ok; ++h) {
             const uint32_t fi = v_fill(fbase, j, h);
-            if constexpr (PG)
-              ok = h > 0 || wwait(bar(B_SLAB_FULL0 + VSLOT_SLAB), tv & 1u);
+            if constexpr (PG)  // the V half that holds this warp's 32 rows
+              ok = h > 0 || wwait(bar(B_SLAB_FULL0 + VSLOT_SLAB + (r >> 6)), tv & 1u);
             else
               ok = wwait(bar((F8 ? B_SLAB_READY0 : B_SLAB_FULL0) + fi % NSLAB),
                          (fi / NSLAB) & 1u);
@@ -879,21 +903,21 @@ cudaError_t launch_prefill(const AttnParams& p, int num_sms,
   }
   const int box_rows = p.block_size < BN ? p.block_size : BN;
   const bool f8 = p.dtype == PKV_FP8_E4M3;
-  // bf16 rows that split into 64-column slabs: page-grouped boxes (a page's
-  // three K slabs in one box, its two V slabs in another); other bf16 rows:
+  // bf16 rows that split into 64-column slabs: page-grouped boxes of up to
+  // 16 keys (a page's three K slabs in one box, its two V slabs in another;
+  // on the 32K causal prefill 3.83-3.89 ms at pages of 16 to 256 keys and
+  // 4.26 ms at 8, against 4.21-5.73 ms for slab fills); other bf16 rows:
   // one 64-column box per slab in the MMAs' 128-byte swizzle; FP8: 64-column
   // boxes of E4M3 codes landing densely, widened in shared memory
-  // page-grouped fills for pages of 8 or 16 keys (measured on the 32K
-  // causal prefill: 4.50 / 4.61 ms against 5.73 / 4.73 ms for slab fills;
-  // from 32-key pages on the multicast slab fills are 2-3 % faster)
   const bool pg = !f8 && p.row_elems % 64 == 0 && p.k_off % 64 == 0 && p.v_off % 64 == 0 &&
-                  box_rows % 8 == 0 && p.block_size <= 16;
+                  box_rows % 8 == 0;
   alignas(64) CUtensorMap v_map;
   if (pg) {
+    const int pg_rows = p.block_size < 16 ? p.block_size : 16;  // as in the kernel
     if (!make_cache_tmap_groups(&kv_map, p.cache, p.layout, p.num_blocks, p.block_size,
-                                p.num_kv_heads, p.row_elems, KSLABS, box_rows) ||
+                                p.num_kv_heads, p.row_elems, KSLABS, pg_rows) ||
         !make_cache_tmap_groups(&v_map, p.cache, p.layout, p.num_blocks, p.block_size,
-                                p.num_kv_heads, p.row_elems, VSLABS, box_rows))
+                                p.num_kv_heads, p.row_elems, VSLABS, pg_rows))
       return cudaErrorInvalidValue;
   } else {
     if (!make_cache_tmap(&kv_map, p.cache, p.dtype, p.layout, p.num_blocks,

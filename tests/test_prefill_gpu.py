@@ -53,8 +53,8 @@ CASES = {
         seed=8),
     "scaled-scores": lambda: wl.make_workload(
         "hot", seq_lens=[400], q_lens=[400], softmax_scale=0.5, seed=9),
-    # page-grouped fills (pages of 8 or 16 keys) with other geometries: 8-key
-    # pages in NHD, V ahead of K in the row; 32-key pages take slab fills
+    # page-grouped fills with other geometries: 8-key pages in NHD (8-key
+    # boxes), 32-key pages (two 16-key boxes a page), V ahead of K in the row
     "block8-nhd": lambda: wl.make_workload(
         "b8n", seq_lens=[150, 40], q_lens=[150, 17], block_size=8, seed=10),
     "block32": lambda: wl.make_workload(
