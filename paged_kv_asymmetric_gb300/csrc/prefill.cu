@@ -371,9 +371,10 @@ __global__ void __launch_bounds__(F8 ? THREADS_F8 : THREADS, 1)
       ++f;
       return true;
     };
-    // page-grouped fills: tile t's K part (kv_map, slot t & 1) or V part
-    // (v_map, the V slot): one box per page, each CTA loading its own, the
-    // slot's previous use read by this CTA's MMAs first
+    // page-grouped fills: tile t's K part (kv_map, slot t & 1) or one 64-key
+    // half of its V part (v_map, the V slot's slab for that half): one box
+    // per 16 keys of a page (per page when pages are smaller), each CTA
+    // loading its own, the slot's previous use read by this CTA's MMAs first
     uint32_t tk = 0, tv = 0;  // K parts and V parts (both halves) issued
     // vh: the 64-key half of a V part (its boxes and its slab)
     auto fill_part = [&](const Item& it, int kt, bool is_v, int pid, int vh) -> bool {
