@@ -171,8 +171,9 @@ int pkv_kv_cache_write(const void *key, int64_t key_tok_stride,
  * pointers, softmax_scale <= 0 or inconsistent sizes, and when q, cache or
  * out is not device memory of the current device (pinned or mapped host
  * memory, managed memory, another GPU's memory): the kernel's tensor maps
- * and its K/V loads, multicast to the two CTAs of a cluster, cover this
- * GPU's own memory only.
+ * and its K/V loads (for FP8 caches and rows that do not split into
+ * 64-column slabs, multicast to the two CTAs of a cluster) cover this GPU's
+ * own memory only.
  */
 int pkv_paged_attn_prefill(const void *q, int num_q_heads, int num_tokens,
                            const void *cache, const pkv_cache_desc *d,

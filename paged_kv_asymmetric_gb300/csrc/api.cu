@@ -141,8 +141,8 @@ bool aligned16(const void* p) {
 }
 
 // Whether every pointer is plain device memory of the current device.  The
-// prefill's tensor maps and its cluster-multicast TMA loads must cover this
-// GPU's own memory only: pinned or mapped host memory, managed memory and a
+// prefill's tensor maps and its TMA loads (cluster-multicast ones among
+// them) must cover this GPU's own memory only: pinned or mapped host memory, managed memory and a
 // peer GPU's memory are refused before any tensor map is encoded.
 int check_local_device(std::initializer_list<const void*> ptrs) {
   int dev = 0;
@@ -242,8 +242,8 @@ int prefill_impl(const void* q, int num_q_heads, int num_tokens, const void* cac
       d->k_off % 64 != 0 || (d->v_off * esz) % 16 != 0)
     return PKV_EUNSUPPORTED;
   if (num_tokens == 0 || num_seqs == 0) return PKV_OK;
-  // q and the cache are read through tensor maps (K/V boxes multicast to
-  // both CTAs of a cluster), out is written: all must be this GPU's memory
+  // q and the cache are read through tensor maps (some K/V boxes multicast
+  // to both CTAs of a cluster), out is written: all must be this GPU's memory
   rc = check_local_device({q, cache, out});
   if (rc != PKV_OK) return rc;
   int* err = nullptr;
